@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark of the grouped-tril masked softmax (forward + backward) on GB300.
+
+One step = the whole hot path over one batch: gtms_forward (mask, scale,
+softmax, zero tail) then gtms_backward on its output, both through the C ABI
+on inputs already resident in HBM. The default workload is
+X[12,64,1000,1000] fp32 ~N(0,1), seq_len ~ U{500..1000}, scale 1, dY ~N(0,1):
+the README's A10 shape, and the largest listed single-GPU workload that runs
+both directions at S = 1000.
+
+Throughput is effective bandwidth on the bytes the method must move
+(e = element bytes, live(L) = L(L+1)/2 kept entries per (b, m) slice):
+  forward  e * sum_{b,m} (live(L_b) + S^2)     kept x read + every y written
+  backward e * sum_{b,m} (2 live(L_b) + S^2)   kept y, dy read + every dx written
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gtms|reference]
+Under torchrun (N > 1) each rank runs its own replica of the workload (rows are
+independent; no collective on the data path) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "masked-softmax fwd/bwd effective GB/s & % GB300 HBM peak; ms per [B,M,S,S] call"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "s1000_b12"
+
+
+# ---------------------------------------------------------------------------
+# Byte model
+# ---------------------------------------------------------------------------
+
+def required_bytes(w, lens):
+    """(forward bytes, backward bytes) the method must move for one call each."""
+    S, e = w.S, w.elem_bytes
+    live = 0
+    for L in lens:
+        L = min(max(int(L), 0), S)
+        live += L * (L + 1) // 2
+    live *= w.M
+    dense = w.B * w.M * S * S
+    fwd = e * (live + dense)
+    bwd = e * (2 * live + dense) if w.backward else 0
+    return fwd, bwd
+
+
+# ---------------------------------------------------------------------------
+# Peaks, traffic records, clocks
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        v = peaks.get("hbm_gbs")
+        if isinstance(v, dict):
+            v = v.get("value", v.get("burst"))
+        if isinstance(v, (int, float)) and v > 0:
+            return float(v), "measured"
+    except (OSError, ValueError, AttributeError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    import glob
+
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "masked_softmax_attention_gb300", "csrc", "*")))
+    for p in files:
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when there is none or the kernel sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha()
+    with open(path) as f:
+        for line in f:
+            if not line.startswith("traffic "):
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split()[1:] if "=" in tok)
+            if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("source_sha") == sha:
+                return int(float(kv["dram_bytes_per_launch"]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in a thread."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.error = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as exc:
+            self.error = f"nvidia-smi unavailable: {exc}"
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.error:
+            return {"error": self.error}
+        rows = []
+        for t, line in self.samples:
+            if t0 <= t <= t1:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 7:
+                    rows.append(parts)
+        if not rows:
+            return {"error": "no nvidia-smi sample inside the timed region"}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle legs
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, lens, slices, device="cpu"):
+    """Inputs of `slices` (b, m) slices of workload w, as raw bits, drawn on the CPU."""
+    import numpy as np
+
+    import seeded_inputs as si
+
+    picked = [b for b, _ in slices]
+    ws = si.Workload(w.name + "_sample", len(picked), 1, w.S, w.dtype, w.scale, x_std=w.x_std,
+                     fixed_seq_lens=tuple(int(lens[b]) for b in picked), spike_prob=w.spike_prob,
+                     spike_value=w.spike_value, backward=w.backward, seed=w.seed + 7)
+    x = si.make_x(ws, device)
+    dy = si.make_dy(ws, device)
+    bits_t = {"f32": (np.uint32, "int32"), "bf16": (np.uint16, "int16"), "f16": (np.uint16, "int16")}[w.dtype]
+    import torch
+
+    tview = getattr(torch, bits_t[1])
+    xb = x.view(tview).numpy().view(bits_t[0])
+    dyb = dy.view(tview).numpy().view(bits_t[0])
+    return ws, xb, dyb
+
+
+def oracle_step(ws, xb, dyb, threads):
+    """One oracle pass over the sample: forward, round, backward (all rows)."""
+    import numpy as np
+
+    import oracle
+
+    lens = np.array(ws.fixed_seq_lens, dtype=np.int32)
+    y = oracle.forward(xb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
+    yb = oracle.round_to(y, ws.dtype_code)
+    if ws.backward:
+        dx = oracle.backward(yb, dyb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
+        oracle.round_to(dx, ws.dtype_code)
+
+
+def cpu_baseline(w, lens, budget_s=12.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of the
+    workload: groups of (b, m) slices until about budget_s of wall time."""
+    threads = os.cpu_count() or 1
+    group = max(1, min(16, w.B * w.M))
+    done_slices, total_bytes, total_s, groups = 0, 0, 0.0, 0
+    while total_s < budget_s and done_slices < w.B * w.M:
+        slices = [((done_slices + i) % w.B, 0) for i in range(group)]
+        ws, xb, dyb = oracle_sample(w, lens, slices)
+        t0 = time.perf_counter()
+        oracle_step(ws, xb, dyb, threads)
+        total_s += time.perf_counter() - t0
+        fb, bb = required_bytes(ws, ws.fixed_seq_lens)
+        total_bytes += fb + bb
+        done_slices += group
+        groups += 1
+    return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done_slices} (b,m) slices of {w.name} (S={w.S}, the workload's seq_lens and value "
+                      f"distribution, drawn on the CPU) in {groups} groups: oracle forward + round + backward, "
+                      f"{total_s:.2f} s wall on {threads} threads"}
+
+
+def run_reference(args, w, lens):
+    """The oracle as the reference arm: K timed steps of a bounded sample each."""
+    import numpy as np  # noqa: F401
+
+    threads = os.cpu_count() or 1
+    ws, xb, dyb = oracle_sample(w, lens, [(0, 0)])
+    for _ in range(args.warmup):
+        oracle_step(ws, xb, dyb, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(ws, xb, dyb, threads)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    fb, bb = required_bytes(ws, ws.fixed_seq_lens)
+    value = (fb + bb) / dt / 1e9
+    sample = (f"1 (b,m) slice of {w.name} per step (S={w.S}, seq_len={ws.fixed_seq_lens[0]}, drawn on the "
+              f"CPU): oracle forward + round + backward")
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic", "config": workload_config(w, lens),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def workload_config(w, lens):
+    fb, bb = required_bytes(w, lens)
+    return {"workload": w.name + ": " + w.describe(), "B": w.B, "M": w.M, "S": w.S, "dtype": w.dtype,
+            "scale": w.scale, "seq_lens_seeded": [int(v) for v in lens] if len(lens) <= 16 else "see seed",
+            "seed": w.seed, "required_bytes_fwd": fb, "required_bytes_bwd": bb,
+            "l2": "no flush: x, y, dy, dx are each larger than the 129 MB L2",
+            "parallelism": "one replica per GPU (rows independent, no collective)"}
+
+
+def run_gpu(args, w, lens, rank, world, local_rank):
+    import torch
+
+    import masked_softmax_attention_gb300 as gtms
+    import seeded_inputs as si
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    gtms.load_library()
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    # per-rank replica: same shape, seed offset by rank
+    wr = si.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank}) if rank else w
+    lens_r = si.seq_lens(wr)
+    x = si.make_x(wr, dev)
+    dy = si.make_dy(wr, dev)
+    lens_d = torch.from_numpy(lens_r).to(dev)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    B, M, S, code, scale = wr.B, wr.M, wr.S, wr.dtype_code, float(wr.scale)
+    xp, yp, dyp, dxp, lp = x.data_ptr(), y.data_ptr(), dy.data_ptr(), dx.data_ptr(), lens_d.data_ptr()
+    fwd_c, bwd_c = gtms.load_library().gtms_forward, gtms.load_library().gtms_backward
+
+    def step():
+        rc = fwd_c(xp, yp, lp, B, M, S, scale, code, sp)
+        if rc:
+            raise gtms.GtmsError("gtms_forward", rc)
+        if wr.backward:
+            rc = bwd_c(yp, dyp, dxp, lp, B, M, S, scale, code, sp)
+            if rc:
+                raise gtms.GtmsError("gtms_backward", rc)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        rc = fwd_c(xp, yp, lp, B, M, S, scale, code, sp)
+        ev[k][1].record(stream)
+        if wr.backward:
+            rc |= bwd_c(yp, dyp, dxp, lp, B, M, S, scale, code, sp)
+        ev[k][2].record(stream)
+        if rc:
+            raise RuntimeError("libgtms call failed inside the timed region")
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev) if wr.backward else 0.0
+    ms_step = total_ms / K
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+
+    fb, bb = required_bytes(wr, lens_r)
+    step_bytes = fb + bb
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+
+    peak, peak_kind = hbm_peak()
+    kern = {}
+    for name, nbytes, ms, direction in (("forward", fb, fwd_ms, 0), ("backward", bb, bwd_ms, 1)):
+        if nbytes == 0:
+            continue
+        kname = gtms.kernel_name(direction, S, code, True)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        kern[name] = {"kernel": kname, "ms_per_call": round(ms, 5), "required_bytes": nbytes,
+                      "achieved_gbs": round(gbs, 2), "frac_of_peak": round(gbs / peak, 4)}
+    dom = max(kern, key=lambda k: kern[k]["ms_per_call"])
+    dk = kern[dom]
+    traffic = recorded_traffic(dk["kernel"], wr.name)
+    roofline = {"bound": "hbm", "kernel": dk["kernel"], "achieved": dk["achieved_gbs"], "peak": peak,
+                "unit": "GB/s", "frac": dk["frac_of_peak"], "traffic": traffic,
+                "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'recipe fallback 6.8 TB/s'})",
+                "algorithmic_bytes_per_launch": dk["required_bytes"]}
+
+    e2e = run_e2e(args, wr, lens_r, dev, stream, fwd_c, bwd_c) if args.e2e_steps > 0 else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, lens)
+    if sampler:
+        sampler.stop()
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+                "config": workload_config(w, lens), "pct_hbm_peak": round(100 * (value / world) / peak, 2),
+                "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": K * (2 if wr.backward else 1), "clocks": clocks,
+                "impl": "gtms"}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, lens, dev, stream, fwd_c, bwd_c):
+    """Same step through the public API with the inputs in pinned host memory:
+    H2D of x, dy, seq_lens and D2H of y, dx inside the timed region."""
+    import torch
+
+    host = {}
+    try:
+        x_h = torch.empty((w.B, w.M, w.S, w.S), dtype=w.torch_dtype, pin_memory=True)
+        dy_h = torch.empty_like(x_h, pin_memory=True)
+        y_h = torch.empty_like(x_h, pin_memory=True)
+        dx_h = torch.empty_like(x_h, pin_memory=True) if w.backward else None
+    except RuntimeError as exc:
+        return {"error": f"pinned host buffers unavailable: {exc}"}
+    import seeded_inputs as si
+
+    x_h.copy_(si.make_x(w, dev))
+    dy_h.copy_(si.make_dy(w, dev))
+    lens_h = torch.from_numpy(lens).pin_memory()
+    x_d, dy_d = torch.empty_like(x_h, device=dev), torch.empty_like(x_h, device=dev)
+    y_d, dx_d = torch.empty_like(x_h, device=dev), torch.empty_like(x_h, device=dev)
+    lens_d = torch.empty_like(lens_h, device=dev)
+    B, M, S, code, scale, sp = w.B, w.M, w.S, w.dtype_code, float(w.scale), stream.cuda_stream
+
+    def step():
+        x_d.copy_(x_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        if w.backward:
+            dy_d.copy_(dy_h, non_blocking=True)
+        rc = fwd_c(x_d.data_ptr(), y_d.data_ptr(), lens_d.data_ptr(), B, M, S, scale, code, sp)
+        if w.backward:
+            rc |= bwd_c(y_d.data_ptr(), dy_d.data_ptr(), dx_d.data_ptr(), lens_d.data_ptr(), B, M, S, scale,
+                        code, sp)
+        y_h.copy_(y_d, non_blocking=True)
+        if w.backward:
+            dx_h.copy_(dx_d, non_blocking=True)
+        if rc:
+            raise RuntimeError("libgtms call failed in the end-to-end loop")
+
+    step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.e2e_steps
+    fb, bb = required_bytes(w, lens)
+    tb = x_h.numel() * x_h.element_size()
+    h2d = tb * (2 if w.backward else 1) + lens_h.numel() * 4
+    d2h = tb * (2 if w.backward else 1)
+    del host
+    return {"value": round((fb + bb) / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "host_buffers": "pinned"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gtms", "reference"], default="gtms")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    import seeded_inputs as si
+
+    w = si.WORKLOADS[args.workload]
+    lens = si.seq_lens(w)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w, lens)
+        return
+    run_gpu(args, w, lens, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,110 @@
+/*
+ * gtms.h -- C ABI of libgtms: the grouped-tril masked softmax over attention
+ * scores, forward and backward, as hand-written CUDA kernels for sm_103a.
+ *
+ * The operation ("Attention-Mask-Optimization" README, section
+ * "算子行为（融合下面的计算）", operator behaviour, and its printed worked
+ * example): X is a contiguous row-major [B, M, S, S] tensor of attention
+ * scores (B batches, M heads, S x S scores per head). For batch b with
+ * valid length L = seq_lens[b], entry (r, c) is kept iff r < L, c < L and
+ * c <= r; the same mask applies to every head. The kept entries of each row
+ * are passed through a softmax of scale * x ("优化ScaledMaskSoftmax算子",
+ * section 4.1: the scale sits inside the exponent); every masked entry is
+ * written as +0.0, and rows r >= L are all +0.0. The mask is computed from
+ * (r, c, seq_lens[b]) inside the kernel and never read from memory (the
+ * README's implementation idea, "实现思路"); masked inputs are never loaded.
+ *
+ * The backward ("ops(8): self-attention 的 CUDA 实现及优化 (下)", section 2.1,
+ * Softmax 求导: dy_i/dx_j = y_i (delta_ij - y_j); section 2.2 applies the scale
+ * in the softmax backward) is dx = scale * y * (dy - rowsum(dy * y)) on kept
+ * entries and +0.0 on masked ones.
+ *
+ * Values of seq_lens outside [0, S] are clamped to that range in the kernel.
+ * Arithmetic is fp32 for every IO dtype; outputs are rounded to the IO dtype
+ * to nearest, ties to even.
+ *
+ * Ownership and threading. The caller owns every buffer. All tensor
+ * pointers are DEVICE pointers on the current CUDA device; seq_lens is a
+ * device int32[B]. The library allocates nothing, keeps no per-call state, is
+ * safe to call from several host threads, and never synchronises: work is
+ * enqueued on `stream` (a cudaStream_t passed as void*; NULL is the legacy
+ * default stream) and the call returns at once. The host never reads
+ * seq_lens.
+ *
+ * Aliasing. Outputs may alias an input exactly (y == x; dx == dy or
+ * dx == y): each row is read before that row is written. Partial overlap of
+ * an output with any input, or of seq_lens with an output, is rejected.
+ *
+ * Errors are returned, never raised, trapped or printed:
+ *   GTMS_OK              work enqueued (or nothing to do: B*M*S == 0).
+ *   GTMS_ERR_INVALID_ARG null pointer with B*M*S > 0, B/M/S < 0, a size whose
+ *                        byte count overflows, a non-finite scale, a pointer
+ *                        not aligned to its element size, partial overlap.
+ *   GTMS_ERR_UNSUPPORTED unknown dtype, or S > GTMS_MAX_S.
+ *   GTMS_ERR_CUDA        the kernel launch failed (cudaGetLastError()).
+ * All argument checks run on the host before anything is enqueued; a call
+ * that returns an error has enqueued nothing.
+ */
+#ifndef GTMS_H
+#define GTMS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GTMS_VERSION 1
+#define GTMS_MAX_S 8192
+
+typedef enum { GTMS_F32 = 0, GTMS_BF16 = 1, GTMS_F16 = 2 } gtms_dtype;
+
+typedef enum {
+    GTMS_OK = 0,
+    GTMS_ERR_INVALID_ARG = 1,
+    GTMS_ERR_UNSUPPORTED = 2,
+    GTMS_ERR_CUDA = 3
+} gtms_status;
+
+/*
+ * Forward: y = grouped-tril masked softmax(scale * x).
+ *   x        device, [B, M, S, S] of `dtype`, read-only; only the kept prefix
+ *            x[b, m, r, 0 : min(r + 1, L)] of rows r < L is loaded.
+ *   y        device, [B, M, S, S] of `dtype`, every element written.
+ *   seq_lens device, int32[B].
+ *   scale    finite float, applied inside the exponent.
+ *   dtype    gtms_dtype of x and y.
+ *   stream   cudaStream_t or NULL.
+ */
+int gtms_forward(const void* x, void* y, const int32_t* seq_lens,
+                 int64_t B, int64_t M, int64_t S, float scale, int dtype, void* stream);
+
+/*
+ * Backward: dx = scale * y * (dy - rowsum(dy * y)) under the same mask.
+ *   y, dy    device, [B, M, S, S] of `dtype`, read-only (y is the forward
+ *            output); only the kept prefix of each live row is loaded.
+ *   dx       device, [B, M, S, S] of `dtype`, every element written.
+ *   Other arguments as in gtms_forward.
+ */
+int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_lens,
+                  int64_t B, int64_t M, int64_t S, float scale, int dtype, void* stream);
+
+/* Static, NUL-terminated name of a status code ("GTMS_OK", ...). */
+const char* gtms_status_string(int status);
+
+/* GTMS_VERSION of the built library. */
+int gtms_version(void);
+
+/*
+ * Name of the kernel variant that gtms_forward (direction 0) or
+ * gtms_backward (direction 1) launches for this row length, dtype and
+ * alignment (aligned16 != 0: every pointer is 16-byte aligned). Static string;
+ * "none" for unsupported arguments. Host-only, enqueues nothing.
+ */
+const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GTMS_H */

@@ -1,0 +1,193 @@
+"""Grouped-tril masked softmax for GB300 (sm_103a): thin Python binding of libgtms.
+
+The compute runs in hand-written CUDA kernels behind the C ABI of
+``include/gtms.h``. This module only marshals arguments: it passes device
+pointers, sizes and the current CUDA stream to ``gtms_forward`` /
+``gtms_backward`` and turns a non-zero status into an exception. There is no
+CPU or PyTorch fallback: if ``libgtms.so`` is missing or cannot be loaded,
+every call raises.
+
+Operation ("Attention-Mask-Optimization" README, operator behaviour): for
+X[B,M,S,S] and per-batch lengths L_b = seq_lens[b], row r keeps columns
+c <= r when r < L_b; kept entries get softmax(scale * x), the rest +0.0.
+Backward ("ops(8): self-attention 的 CUDA 实现及优化 (下)", section 2.1):
+dx = scale * y * (dy - rowsum(dy * y)) on kept entries, +0.0 elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_PATH, build_library  # noqa: F401  (re-exported for build scripts)
+
+GTMS_F32, GTMS_BF16, GTMS_F16 = 0, 1, 2
+GTMS_OK, GTMS_ERR_INVALID_ARG, GTMS_ERR_UNSUPPORTED, GTMS_ERR_CUDA = 0, 1, 2, 3
+GTMS_MAX_S = 8192
+
+EXPORTED_SYMBOLS = ("gtms_forward", "gtms_backward", "gtms_status_string", "gtms_version",
+                    "gtms_kernel_name")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GtmsError(RuntimeError):
+    """A libgtms call returned a non-zero status."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load libgtms.so (built in-tree by ``build_library``); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libgtms.so not found at {p}: build it with "
+                               "masked_softmax_attention_gb300.build_library() (needs nvcc); "
+                               "there is no fallback implementation")
+        lib = ctypes.CDLL(p)
+        vp, i64 = ctypes.c_void_p, ctypes.c_int64
+        lib.gtms_forward.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
+        lib.gtms_forward.restype = ctypes.c_int
+        lib.gtms_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
+        lib.gtms_backward.restype = ctypes.c_int
+        lib.gtms_status_string.argtypes = [ctypes.c_int]
+        lib.gtms_status_string.restype = ctypes.c_char_p
+        lib.gtms_version.argtypes = []
+        lib.gtms_version.restype = ctypes.c_int
+        lib.gtms_kernel_name.argtypes = [ctypes.c_int, i64, ctypes.c_int, ctypes.c_int]
+        lib.gtms_kernel_name.restype = ctypes.c_char_p
+        if path is None:
+            _lib = lib
+        return lib
+
+
+# ---------------------------------------------------------------------------
+# Raw C-ABI calls: integer pointers in, status code out.
+# ---------------------------------------------------------------------------
+
+def gtms_forward(x, y, seq_lens, B, M, S, scale, dtype, stream) -> int:
+    return load_library().gtms_forward(x, y, seq_lens, B, M, S, scale, dtype, stream)
+
+
+def gtms_backward(y, dy, dx, seq_lens, B, M, S, scale, dtype, stream) -> int:
+    return load_library().gtms_backward(y, dy, dx, seq_lens, B, M, S, scale, dtype, stream)
+
+
+def status_string(status: int) -> str:
+    return load_library().gtms_status_string(status).decode()
+
+
+def gtms_version() -> int:
+    return load_library().gtms_version()
+
+
+def kernel_name(direction: int, S: int, dtype: int, aligned16: bool = True) -> str:
+    return load_library().gtms_kernel_name(direction, S, dtype, 1 if aligned16 else 0).decode()
+
+
+# ---------------------------------------------------------------------------
+# Tensor API (torch provides device memory and the stream, nothing else).
+# ---------------------------------------------------------------------------
+
+def _dtype_code(t) -> int:
+    import torch
+
+    codes = {torch.float32: GTMS_F32, torch.bfloat16: GTMS_BF16, torch.float16: GTMS_F16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}; expected float32, bfloat16 or float16")
+    return codes[t.dtype]
+
+
+def _check_scores(name, t):
+    if t.dim() != 4 or t.shape[-1] != t.shape[-2]:
+        raise ValueError(f"{name} must be [B, M, S, S], got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_lens(seq_lens, B, device):
+    import torch
+
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != (B,) or seq_lens.device != device \
+            or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 CUDA tensor of shape [B] on the scores' device")
+
+
+def forward(x, seq_lens, scale: float = 1.0, out=None):
+    """y = grouped-tril masked softmax(scale * x); ``out`` may be ``x`` (in place)."""
+    import torch
+
+    _check_scores("x", x)
+    B, M, S, _ = x.shape
+    _check_lens(seq_lens, B, x.device)
+    y = torch.empty_like(x) if out is None else out
+    if y.shape != x.shape or y.dtype != x.dtype or y.device != x.device or not y.is_contiguous():
+        raise ValueError("out must match x in shape, dtype, device and be contiguous")
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    rc = gtms_forward(x.data_ptr(), y.data_ptr(), seq_lens.data_ptr(), B, M, S, float(scale),
+                      _dtype_code(x), stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_forward", rc)
+    return y
+
+
+def backward(y, dy, seq_lens, scale: float = 1.0, out=None):
+    """dx = scale * y * (dy - rowsum(dy * y)) under the mask; ``out`` may be ``y`` or ``dy``."""
+    import torch
+
+    _check_scores("y", y)
+    _check_scores("dy", dy)
+    if dy.shape != y.shape or dy.dtype != y.dtype or dy.device != y.device:
+        raise ValueError("dy must match y in shape, dtype and device")
+    B, M, S, _ = y.shape
+    _check_lens(seq_lens, B, y.device)
+    dx = torch.empty_like(y) if out is None else out
+    if dx.shape != y.shape or dx.dtype != y.dtype or dx.device != y.device or not dx.is_contiguous():
+        raise ValueError("out must match y in shape, dtype, device and be contiguous")
+    stream = torch.cuda.current_stream(y.device).cuda_stream
+    rc = gtms_backward(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), seq_lens.data_ptr(), B, M, S,
+                       float(scale), _dtype_code(y), stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_backward", rc)
+    return dx
+
+
+def _autograd_function():
+    import torch
+
+    class GroupedTrilMaskSoftmax(torch.autograd.Function):
+        """Autograd wrapper: forward and backward both run the CUDA kernels."""
+
+        @staticmethod
+        def forward(ctx, x, seq_lens, scale):
+            y = forward(x.contiguous(), seq_lens, scale)
+            ctx.save_for_backward(y, seq_lens)
+            ctx.scale = scale
+            return y
+
+        @staticmethod
+        def backward(ctx, dy):
+            y, seq_lens = ctx.saved_tensors
+            return backward(y, dy.contiguous(), seq_lens, ctx.scale), None, None
+
+    return GroupedTrilMaskSoftmax
+
+
+_fn = None
+
+
+def grouped_tril_mask_softmax(x, seq_lens, scale: float = 1.0):
+    """Differentiable op: ``y = grouped_tril_mask_softmax(x, seq_lens, scale)``."""
+    global _fn
+    if _fn is None:
+        _fn = _autograd_function()
+    return _fn.apply(x, seq_lens, float(scale))

@@ -1,0 +1,206 @@
+// gtms_api.cu -- the C ABI declared in include/gtms.h: host-side argument
+// checks, variant choice and kernel launch. No allocation, no synchronisation,
+// no host read of device memory.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "gtms.h"
+#include "gtms_dispatch.h"
+#include "gtms_kernels.cuh"
+
+#define GTMS_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace gtms {
+template <typename T>
+void launch_forward(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+template <typename T>
+void launch_backward(int, const void*, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+extern template void launch_forward<float>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+extern template void launch_forward<__nv_bfloat16>(int, const void*, void*, const int32_t*, const Geom&, float,
+                                                   cudaStream_t);
+extern template void launch_forward<__half>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+extern template void launch_backward<float>(int, const void*, const void*, void*, const int32_t*, const Geom&, float,
+                                            cudaStream_t);
+extern template void launch_backward<__nv_bfloat16>(int, const void*, const void*, void*, const int32_t*,
+                                                    const Geom&, float, cudaStream_t);
+extern template void launch_backward<__half>(int, const void*, const void*, void*, const int32_t*, const Geom&,
+                                             float, cudaStream_t);
+}  // namespace gtms
+
+namespace {
+
+int elem_bytes(int dtype)
+{
+    switch (dtype) {
+    case GTMS_F32: return 4;
+    case GTMS_BF16:
+    case GTMS_F16: return 2;
+    default: return 0;
+    }
+}
+
+struct Checked {
+    int status;
+    int64_t rows;
+    uint64_t bytes;   // bytes of one [B,M,S,S] tensor
+};
+
+// Shape, scale and dtype checks shared by both directions.
+Checked check_shape(int64_t B, int64_t M, int64_t S, float scale, int dtype)
+{
+    Checked c{GTMS_OK, 0, 0};
+    if (B < 0 || M < 0 || S < 0 || !std::isfinite(scale)) {
+        c.status = GTMS_ERR_INVALID_ARG;
+        return c;
+    }
+    const int e = elem_bytes(dtype);
+    if (e == 0 || S > GTMS_MAX_S) {
+        c.status = GTMS_ERR_UNSUPPORTED;
+        return c;
+    }
+    int64_t rows = 0, elems = 0, bytes = 0;
+    if (__builtin_mul_overflow(B, M, &rows) || __builtin_mul_overflow(rows, S, &rows) ||
+        __builtin_mul_overflow(rows, S, &elems) || __builtin_mul_overflow(elems, static_cast<int64_t>(e), &bytes) ||
+        B > INT32_MAX) {
+        c.status = GTMS_ERR_INVALID_ARG;
+        return c;
+    }
+    c.rows = rows;
+    c.bytes = static_cast<uint64_t>(bytes);
+    return c;
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, uint64_t an, const void* b, uint64_t bn)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bn && b0 < a0 + an;
+}
+
+// An output may equal an input exactly; any other overlap is rejected.
+bool bad_alias(const void* out, const void* in, uint64_t bytes)
+{
+    return out != in && overlaps(out, bytes, in, bytes);
+}
+
+gtms::Geom make_geom(int64_t rows, int64_t M, int64_t S, int variant, int e)
+{
+    const gtms::Variant& v = gtms::variant_at(variant);
+    gtms::Geom g;
+    g.rows = rows;
+    g.rows_per_b = M * S;
+    g.S = static_cast<int32_t>(S);
+    g.units = static_cast<int32_t>(v.vec16 ? S * e / 16 : S);
+    g.small = rows <= static_cast<int64_t>(UINT32_MAX) ? 1 : 0;
+    return g;
+}
+
+int launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? GTMS_OK : GTMS_ERR_CUDA;
+}
+
+}  // namespace
+
+GTMS_EXPORT int gtms_forward(const void* x, void* y, const int32_t* seq_lens, int64_t B, int64_t M, int64_t S,
+                             float scale, int dtype, void* stream)
+{
+    const Checked c = check_shape(B, M, S, scale, dtype);
+    if (c.status != GTMS_OK || c.rows == 0)
+        return c.status;
+    const int e = elem_bytes(dtype);
+    if (!x || !y || !seq_lens)
+        return GTMS_ERR_INVALID_ARG;
+    if (!aligned_to(x, e) || !aligned_to(y, e) || !aligned_to(seq_lens, 4))
+        return GTMS_ERR_INVALID_ARG;
+    const uint64_t lens_bytes = static_cast<uint64_t>(B) * 4;
+    if (bad_alias(y, x, c.bytes) || overlaps(y, c.bytes, seq_lens, lens_bytes))
+        return GTMS_ERR_INVALID_ARG;
+
+    const bool a16 = aligned_to(x, 16) && aligned_to(y, 16);
+    const int variant = gtms::pick_variant(S, e, a16);
+    if (variant < 0)
+        return GTMS_ERR_UNSUPPORTED;
+    const gtms::Geom g = make_geom(c.rows, M, S, variant, e);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case GTMS_F32: gtms::launch_forward<float>(variant, x, y, seq_lens, g, scale, st); break;
+    case GTMS_BF16: gtms::launch_forward<__nv_bfloat16>(variant, x, y, seq_lens, g, scale, st); break;
+    default: gtms::launch_forward<__half>(variant, x, y, seq_lens, g, scale, st); break;
+    }
+    return launch_status();
+}
+
+GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B, int64_t M,
+                              int64_t S, float scale, int dtype, void* stream)
+{
+    const Checked c = check_shape(B, M, S, scale, dtype);
+    if (c.status != GTMS_OK || c.rows == 0)
+        return c.status;
+    const int e = elem_bytes(dtype);
+    if (!y || !dy || !dx || !seq_lens)
+        return GTMS_ERR_INVALID_ARG;
+    if (!aligned_to(y, e) || !aligned_to(dy, e) || !aligned_to(dx, e) || !aligned_to(seq_lens, 4))
+        return GTMS_ERR_INVALID_ARG;
+    const uint64_t lens_bytes = static_cast<uint64_t>(B) * 4;
+    if (bad_alias(dx, y, c.bytes) || bad_alias(dx, dy, c.bytes) || overlaps(dx, c.bytes, seq_lens, lens_bytes))
+        return GTMS_ERR_INVALID_ARG;
+
+    const bool a16 = aligned_to(y, 16) && aligned_to(dy, 16) && aligned_to(dx, 16);
+    const int variant = gtms::pick_variant(S, e, a16);
+    if (variant < 0)
+        return GTMS_ERR_UNSUPPORTED;
+    const gtms::Geom g = make_geom(c.rows, M, S, variant, e);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case GTMS_F32: gtms::launch_backward<float>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    case GTMS_BF16: gtms::launch_backward<__nv_bfloat16>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    default: gtms::launch_backward<__half>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    }
+    return launch_status();
+}
+
+GTMS_EXPORT const char* gtms_status_string(int status)
+{
+    switch (status) {
+    case GTMS_OK: return "GTMS_OK";
+    case GTMS_ERR_INVALID_ARG: return "GTMS_ERR_INVALID_ARG";
+    case GTMS_ERR_UNSUPPORTED: return "GTMS_ERR_UNSUPPORTED";
+    case GTMS_ERR_CUDA: return "GTMS_ERR_CUDA";
+    default: return "GTMS_UNKNOWN_STATUS";
+    }
+}
+
+GTMS_EXPORT int gtms_version(void) { return GTMS_VERSION; }
+
+GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16)
+{
+    static const char* const kDtype[3] = {"f32", "bf16", "f16"};
+    constexpr int kVariants = gtms::kNumVec + gtms::kNumElem;
+    // [direction][dtype][variant], filled once (thread-safe static initialisation).
+    struct Names {
+        char text[2][3][kVariants][64];
+        Names()
+        {
+            for (int d = 0; d < 2; ++d)
+                for (int t = 0; t < 3; ++t)
+                    for (int v = 0; v < kVariants; ++v) {
+                        const gtms::Variant& var = gtms::variant_at(v);
+                        std::snprintf(text[d][t][v], sizeof text[d][t][v], "gtms_%s_kernel<%s,%s,team%d,x%d>",
+                                      d == 0 ? "fwd" : "bwd", kDtype[t], var.vec16 ? "vec16" : "elem", var.team,
+                                      var.per_thread);
+                    }
+        }
+    };
+    static const Names names;
+    const int e = elem_bytes(dtype);
+    if ((direction != 0 && direction != 1) || e == 0 || S < 1 || S > GTMS_MAX_S)
+        return "none";
+    const int v = gtms::pick_variant(S, e, aligned16 != 0);
+    return v < 0 ? "none" : names.text[direction][dtype][v];
+}

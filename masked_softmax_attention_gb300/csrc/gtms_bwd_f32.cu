@@ -1,0 +1,7 @@
+// Backward kernel instantiations for f32 IO.
+#include "gtms_launch.cuh"
+
+namespace gtms {
+template void launch_backward<float>(int, const void*, const void*, void*, const int32_t*, const Geom&, float,
+                                   cudaStream_t);
+}  // namespace gtms

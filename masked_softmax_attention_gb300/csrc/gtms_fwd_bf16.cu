@@ -1,0 +1,6 @@
+// Forward kernel instantiations for bf16 IO.
+#include "gtms_launch.cuh"
+
+namespace gtms {
+template void launch_forward<__nv_bfloat16>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+}  // namespace gtms

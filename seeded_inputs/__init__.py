@@ -1,0 +1,185 @@
+"""Seeded synthetic inputs for the grouped-tril masked softmax workloads.
+
+This module draws random numbers and nothing else: it holds none of the
+method's arithmetic (no mask, no softmax, no rounding rule of its own). It is
+the one module that both the CUDA-path tests / bench and the CPU oracle take
+inputs from.
+
+Workloads (shapes, dtypes and distributions of the pages' runs):
+
+* ``worked_example`` -- X[3,2,5,5] fp32 ~N(0,1), seq_lens [3,4,5], scale 1,
+  forward only: the printed example of the "Attention-Mask-Optimization"
+  README (operator behaviour section).
+* ``s1000_b3`` -- X[3,64,1000,1000] fp32 ~N(0,1), seq_len ~ U{1..1000},
+  scale 1, forward: the README's DevCloud / A10 shape.
+* ``s1000_b12`` -- X[12,64,1000,1000] fp32 ~N(0,1), seq_len ~ U{500..1000},
+  scale 1, forward + backward with dY ~N(0,1) fp32 (the README's A10 shape).
+* ``s2048_bf16`` -- X[32,16,2048,2048] bf16 ~N(0, variance 4),
+  seq_len ~ U{1024..2048}, scale 0.125 (head_dim 64), forward + backward with
+  dY ~N(0,1) bf16 ("优化ScaledMaskSoftmax算子" section 3.2: batch 32, head_dim 64).
+* ``s8192_f16`` -- X[4,16,8192,8192] fp16 ~N(0,1) with an independent 1%
+  of entries set to +30, seq_len ~ U{4096..8192}, scale 0.125, forward +
+  backward with dY ~N(0,1) fp16 (long rows, overflow stress).
+* ``s4096_bf16`` -- X[32,16,4096,4096] bf16 ~N(0, variance 4),
+  seq_len ~ U{2048..4096}, scale 0.125, forward + backward: an added S=4096
+  measurement point mirroring the ScaledMaskSoftmax article's 4096 row.
+
+Every tensor comes from torch's seeded generators (Philox on CUDA, mt19937 on
+the CPU), drawn in float32 and cast to the IO dtype with round-to-nearest-even.
+The same seed on the same device type gives the same bytes.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+DTYPE_CODES = {"f32": 0, "bf16": 1, "f16": 2}
+TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+ELEM_BYTES = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    M: int
+    S: int
+    dtype: str
+    scale: float
+    x_std: float = 1.0
+    seq_len_range: tuple | None = None      # inclusive (lo, hi), drawn uniformly per batch
+    fixed_seq_lens: tuple | None = None
+    spike_prob: float = 0.0                 # probability that an x entry is replaced by spike_value
+    spike_value: float = 30.0
+    backward: bool = True
+    seed: int = 20261202
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.M * self.S
+
+    @property
+    def elems(self) -> int:
+        return self.B * self.M * self.S * self.S
+
+    @property
+    def dtype_code(self) -> int:
+        return DTYPE_CODES[self.dtype]
+
+    @property
+    def torch_dtype(self):
+        return TORCH_DTYPES[self.dtype]
+
+    @property
+    def elem_bytes(self) -> int:
+        return ELEM_BYTES[self.dtype]
+
+    def describe(self) -> str:
+        if self.fixed_seq_lens is not None:
+            lens = "seq_lens=" + ",".join(str(v) for v in self.fixed_seq_lens)
+        else:
+            lens = f"seq_len~U{{{self.seq_len_range[0]}..{self.seq_len_range[1]}}}"
+        dist = f"N(0,{self.x_std ** 2:g})"
+        if self.spike_prob:
+            dist += f"+{self.spike_prob:g}x{self.spike_value:g}"
+        return (f"X[{self.B},{self.M},{self.S},{self.S}] {self.dtype} {dist} {lens} scale={self.scale:g} "
+                f"{'fwd+bwd' if self.backward else 'fwd'}")
+
+
+WORKLOADS = {
+    "worked_example": Workload("worked_example", 3, 2, 5, "f32", 1.0, fixed_seq_lens=(3, 4, 5),
+                               backward=False, seed=20261203),
+    "s1000_b3": Workload("s1000_b3", 3, 64, 1000, "f32", 1.0, seq_len_range=(1, 1000),
+                         backward=False, seed=20261204),
+    "s1000_b12": Workload("s1000_b12", 12, 64, 1000, "f32", 1.0, seq_len_range=(500, 1000),
+                          seed=20261205),
+    "s2048_bf16": Workload("s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
+                           seq_len_range=(1024, 2048), seed=20261206),
+    "s8192_f16": Workload("s8192_f16", 4, 16, 8192, "f16", 0.125, seq_len_range=(4096, 8192),
+                          spike_prob=0.01, spike_value=30.0, seed=20261207),
+    "s4096_bf16": Workload("s4096_bf16", 32, 16, 4096, "bf16", 0.125, x_std=2.0,
+                           seq_len_range=(2048, 4096), seed=20261208),
+}
+
+
+def custom(name, B, M, S, dtype, scale=1.0, *, seq_lens=None, seq_len_range=None, x_std=1.0,
+           spike_prob=0.0, backward=True, seed=1) -> Workload:
+    """A workload of any shape (tests: ragged tails, edge sizes, odd lengths)."""
+    if seq_lens is None and seq_len_range is None:
+        seq_len_range = (0, S)
+    return Workload(name, B, M, S, dtype, scale, x_std=x_std,
+                    seq_len_range=None if seq_lens is not None else tuple(seq_len_range),
+                    fixed_seq_lens=None if seq_lens is None else tuple(int(v) for v in seq_lens),
+                    spike_prob=spike_prob, backward=backward, seed=seed)
+
+
+def seq_lens(w: Workload) -> np.ndarray:
+    """int32 [B]: fixed lengths, or uniform integers in the inclusive range."""
+    if w.fixed_seq_lens is not None:
+        return np.array(w.fixed_seq_lens, dtype=np.int32)
+    g = torch.Generator().manual_seed(w.seed * 4 + 3)
+    lo, hi = w.seq_len_range
+    return torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64).numpy().astype(np.int32)
+
+
+def _chunks(w: Workload, max_elems: int):
+    slices = w.B * w.M
+    per = max(1, max_elems // max(1, w.S * w.S))
+    for s0 in range(0, slices, per):
+        yield s0, min(slices, s0 + per)
+
+
+def _draw(w: Workload, device, stream_id: int, std: float, spikes: bool, max_chunk_elems: int):
+    dev = torch.device(device)
+    out = torch.empty((w.B, w.M, w.S, w.S), dtype=w.torch_dtype, device=dev)
+    if w.elems == 0:
+        return out
+    g = torch.Generator(device=dev).manual_seed(w.seed * 4 + stream_id)
+    flat = out.view(w.B * w.M, w.S, w.S)
+    for s0, s1 in _chunks(w, max_chunk_elems):
+        shape = (s1 - s0, w.S, w.S)
+        v = torch.randn(shape, generator=g, device=dev, dtype=torch.float32)
+        if std != 1.0:
+            v.mul_(std)
+        if spikes and w.spike_prob > 0:
+            hit = torch.rand(shape, generator=g, device=dev, dtype=torch.float32) < w.spike_prob
+            v.masked_fill_(hit, w.spike_value)
+        flat[s0:s1].copy_(v)
+    return out
+
+
+def make_x(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.Tensor:
+    """Scores X[B,M,S,S] in the workload's dtype."""
+    return _draw(w, device, 0, w.x_std, True, max_chunk_elems)
+
+
+def make_dy(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.Tensor:
+    """Upstream gradient dY[B,M,S,S] ~ N(0,1) in the workload's dtype."""
+    return _draw(w, device, 1, 1.0, False, max_chunk_elems)
+
+
+def make_probs(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.Tensor:
+    """A stand-in Y[B,M,S,S] ~ U[0,1) for backward edge cases whose values need no structure."""
+    dev = torch.device(device)
+    out = torch.empty((w.B, w.M, w.S, w.S), dtype=w.torch_dtype, device=dev)
+    if w.elems == 0:
+        return out
+    g = torch.Generator(device=dev).manual_seed(w.seed * 4 + 2)
+    flat = out.view(w.B * w.M, w.S, w.S)
+    for s0, s1 in _chunks(w, max_chunk_elems):
+        flat[s0:s1].copy_(torch.rand((s1 - s0, w.S, w.S), generator=g, device=dev, dtype=torch.float32))
+    return out
+
+
+def sample_slices(w: Workload, count: int) -> list:
+    """A fixed, seeded choice of (b, m) slices: first, last, and random others."""
+    total = w.B * w.M
+    if total <= count:
+        return [(s // w.M, s % w.M) for s in range(total)]
+    rng = np.random.default_rng(w.seed)
+    picks = {0, total - 1}
+    while len(picks) < count:
+        picks.add(int(rng.integers(0, total)))
+    return [(s // w.M, s % w.M) for s in sorted(picks)]

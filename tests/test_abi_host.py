@@ -1,0 +1,177 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+Every call here fails argument validation, or is an empty no-op, before the
+library touches CUDA; the fake pointer values are never dereferenced. The
+tests check that libgtms.so loads, exports exactly what include/gtms.h
+declares, and maps each kind of bad argument to its documented status.
+"""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+import masked_softmax_attention_gb300 as gtms
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gtms.h")
+
+OK, INVALID, UNSUPPORTED = gtms.GTMS_OK, gtms.GTMS_ERR_INVALID_ARG, gtms.GTMS_ERR_UNSUPPORTED
+F32, BF16, F16 = gtms.GTMS_F32, gtms.GTMS_BF16, gtms.GTMS_F16
+
+# Distinct, 256-byte aligned fake device addresses, far apart. Never dereferenced.
+X, Y, DY, LENS = 0x10_0000_0000, 0x20_0000_0000, 0x30_0000_0000, 0x40_0000_0000
+
+
+def _cuda_visible():
+    import torch
+
+    return torch.cuda.is_available() or os.path.exists("/dev/nvidia0")
+
+
+# These tests hand the library fake device addresses. Each call is meant to be
+# rejected on the host, but on a machine with a GPU a slip in a test would
+# launch a kernel on them, so the module runs only where no GPU is visible.
+pytestmark = pytest.mark.skipif(_cuda_visible(), reason="fake-pointer host tests run only without a GPU")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gtms.build_library()
+    return gtms.load_library()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(gtms_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_public_api():
+    assert declared_functions() == sorted(gtms.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib):
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", gtms.LIB_PATH], capture_output=True, text=True).stdout
+    exported = sorted({ln.split()[-1] for ln in out.splitlines() if " T " in ln and ln.split()[-1].startswith("gtms")})
+    assert exported == declared_functions()
+
+
+def test_version_and_status_strings(lib):
+    assert gtms.gtms_version() == 1
+    assert gtms.status_string(OK) == "GTMS_OK"
+    assert gtms.status_string(INVALID) == "GTMS_ERR_INVALID_ARG"
+    assert gtms.status_string(UNSUPPORTED) == "GTMS_ERR_UNSUPPORTED"
+    assert gtms.status_string(gtms.GTMS_ERR_CUDA) == "GTMS_ERR_CUDA"
+    assert gtms.status_string(99) == "GTMS_UNKNOWN_STATUS"
+
+
+def test_kernel_choice(lib):
+    # warp per row for rows up to 4 KB of 16-byte vectors, a CTA per row beyond
+    assert gtms.kernel_name(0, 1000, F32) == "gtms_fwd_kernel<f32,vec16,team32,x8>"
+    assert gtms.kernel_name(1, 1000, F32) == "gtms_bwd_kernel<f32,vec16,team32,x8>"
+    assert gtms.kernel_name(0, 2048, BF16) == "gtms_fwd_kernel<bf16,vec16,team32,x8>"
+    assert gtms.kernel_name(1, 8192, F16) == "gtms_bwd_kernel<f16,vec16,team256,x4>"
+    assert gtms.kernel_name(0, 8192, F32) == "gtms_fwd_kernel<f32,vec16,team512,x4>"
+    # rows whose byte length is not a multiple of 16, or unaligned buffers: element access
+    assert gtms.kernel_name(0, 5, F32) == "gtms_fwd_kernel<f32,elem,team32,x1>"
+    assert gtms.kernel_name(0, 1000, F32, aligned16=False) == "gtms_fwd_kernel<f32,elem,team32,x32>"
+    assert gtms.kernel_name(0, 8191, F16) == "gtms_fwd_kernel<f16,elem,team256,x32>"
+    # out of range
+    assert gtms.kernel_name(0, 8193, F32) == "none"
+    assert gtms.kernel_name(0, 0, F32) == "none"
+    assert gtms.kernel_name(2, 100, F32) == "none"
+    assert gtms.kernel_name(0, 100, 7) == "none"
+
+
+def fwd(x=X, y=Y, lens=LENS, B=2, M=3, S=64, scale=1.0, dtype=F32):
+    return gtms.gtms_forward(x, y, lens, B, M, S, scale, dtype, None)
+
+
+def bwd(y=X, dy=DY, dx=Y, lens=LENS, B=2, M=3, S=64, scale=1.0, dtype=F32):
+    return gtms.gtms_backward(y, dy, dx, lens, B, M, S, scale, dtype, None)
+
+
+@pytest.mark.parametrize("call", [fwd, bwd])
+def test_shape_and_scale_errors(lib, call):
+    assert call(B=-1) == INVALID
+    assert call(M=-2) == INVALID
+    assert call(S=-5) == INVALID
+    assert call(scale=float("nan")) == INVALID
+    assert call(scale=float("inf")) == INVALID
+    assert call(dtype=3) == UNSUPPORTED
+    assert call(dtype=-1) == UNSUPPORTED
+    assert call(S=gtms.GTMS_MAX_S + 1) == UNSUPPORTED
+    # byte count overflows int64
+    assert call(B=1 << 30, M=1 << 30, S=4096) == INVALID
+
+
+@pytest.mark.parametrize("call", [fwd, bwd])
+def test_empty_work_is_an_ok_noop_even_with_null_pointers(lib, call):
+    if call is fwd:
+        assert fwd(x=None, y=None, lens=None, B=0) == OK
+        assert fwd(x=None, y=None, lens=None, M=0) == OK
+        assert fwd(x=None, y=None, lens=None, S=0) == OK
+    else:
+        assert bwd(y=None, dy=None, dx=None, lens=None, B=0) == OK
+        assert bwd(y=None, dy=None, dx=None, lens=None, S=0) == OK
+
+
+def test_forward_pointer_errors(lib):
+    assert fwd(x=None) == INVALID
+    assert fwd(y=None) == INVALID
+    assert fwd(lens=None) == INVALID
+    assert fwd(x=X + 2) == INVALID                    # fp32 element not 4-byte aligned
+    assert fwd(y=Y + 1, dtype=BF16) == INVALID        # 16-bit element not 2-byte aligned
+    assert fwd(lens=LENS + 2) == INVALID              # int32 seq_lens not 4-byte aligned
+    nbytes = 2 * 3 * 64 * 64 * 4
+    assert fwd(y=X + 16) == INVALID                   # partial overlap of y with x
+    assert fwd(y=X - nbytes + 16) == INVALID
+    assert fwd(lens=Y + nbytes - 4) == INVALID        # seq_lens inside the output
+
+
+def test_backward_pointer_errors(lib):
+    assert bwd(y=None) == INVALID
+    assert bwd(dy=None) == INVALID
+    assert bwd(dx=None) == INVALID
+    assert bwd(lens=None) == INVALID
+    assert bwd(dx=Y + 1, dtype=F16) == INVALID        # 16-bit element not 2-byte aligned
+    nbytes = 2 * 3 * 64 * 64 * 4
+    assert bwd(dx=DY + 64) == INVALID                 # partial overlap with dy
+    assert bwd(dx=X + nbytes - 4) == INVALID          # partial overlap with y
+    assert bwd(lens=Y + 128) == INVALID               # seq_lens inside dx
+    assert bwd(dy=DY + 1) == INVALID
+
+
+def test_tensor_api_rejects_cpu_tensors(lib):
+    import torch
+
+    x = torch.zeros(1, 1, 4, 4)
+    lens = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        gtms.forward(x, lens)
+    with pytest.raises(ValueError):
+        gtms.backward(x, x, lens)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no fallback"):
+        gtms.load_library(str(tmp_path / "libgtms.so"))
+
+
+def test_ctypes_signatures_match_header(lib):
+    text = open(HEADER, encoding="utf-8").read()
+    fwd_decl = re.search(r"int gtms_forward\(([^)]*)\)", text, re.S).group(1)
+    bwd_decl = re.search(r"int gtms_backward\(([^)]*)\)", text, re.S).group(1)
+    assert len(fwd_decl.split(",")) == len(lib.gtms_forward.argtypes) == 9
+    assert len(bwd_decl.split(",")) == len(lib.gtms_backward.argtypes) == 10
+    assert lib.gtms_forward.argtypes[6] is ctypes.c_float

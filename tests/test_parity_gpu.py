@@ -1,0 +1,318 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Element-by-element on seeded inputs at sizes the oracle finishes in seconds
+(several rows per team, ragged kept prefixes, partial 16-byte units), on edge
+sizes, and at the full workload sizes on sampled (b, m) slices plus
+properties checked on every row. Backward inputs y are the oracle's own
+forward output rounded to the IO dtype, never the GPU's.
+"""
+import numpy as np
+import pytest
+import torch
+
+import masked_softmax_attention_gb300 as gtms
+import oracle
+import seeded_inputs as si
+from parity_utils import (Stats, check_backward, check_forward, from_bits, live_row_sums_close_to_one,
+                          masked_bits_all_zero, oracle_forward_bits, row_chunks, to_bits)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gtms.build_library()
+    gtms.load_library()
+    return torch.device("cuda:0")
+
+
+def _lens_dev(w, dev):
+    return torch.from_numpy(si.seq_lens(w)).to(dev)
+
+
+def run_and_check(w, dev, backward=True, x_cpu=None, offset_elems=0):
+    """Full element-wise parity of forward (and backward) for a small workload."""
+    B, M, S = w.B, w.M, w.S
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    x = si.make_x(w, "cpu") if x_cpu is None else x_cpu
+    x_bits = to_bits(x, w.dtype).reshape(-1)
+
+    def place(t):
+        if offset_elems == 0:
+            return t.to(dev)
+        buf = torch.empty(t.numel() + offset_elems, dtype=t.dtype, device=dev)
+        view = buf[offset_elems:].view(t.shape)
+        view.copy_(t)
+        return view
+
+    y = place(torch.zeros_like(x))
+    gtms.forward(place(x), lens_d, w.scale, out=y)
+    torch.cuda.synchronize()
+    y_bits = to_bits(y, w.dtype).reshape(-1)
+    st = Stats()
+    for a, b in row_chunks(0, w.rows, S):
+        check_forward(x_bits[a * S:b * S], y_bits[a * S:b * S], lens, B, M, S, w.scale, w.dtype, a, b, st)
+    assert st.ok, f"forward {w.describe()}: {st}"
+    if not backward:
+        return st, None
+    y_or = oracle_forward_bits(x_bits, lens, B, M, S, w.scale, w.dtype)
+    dy = si.make_dy(w, "cpu")
+    dy_bits = to_bits(dy, w.dtype).reshape(-1)
+    dx = place(torch.zeros_like(dy))
+    gtms.backward(place(from_bits(y_or, w.dtype, "cpu")), place(dy), lens_d, w.scale, out=dx)
+    torch.cuda.synchronize()
+    dx_bits = to_bits(dx, w.dtype).reshape(-1)
+    yb = y_or.reshape(-1)
+    sb = Stats()
+    for a, b in row_chunks(0, w.rows, S):
+        check_backward(yb[a * S:b * S], dy_bits[a * S:b * S], dx_bits[a * S:b * S], lens, B, M, S, w.scale,
+                       w.dtype, a, b, sb)
+    assert sb.ok, f"backward {w.describe()}: {sb}"
+    return st, sb
+
+
+# ---------------------------------------------------------------------------
+# Workload-shaped cases small enough for a full comparison
+# ---------------------------------------------------------------------------
+
+REDUCED = [
+    si.WORKLOADS["worked_example"],
+    si.custom("s1000_f32", 2, 3, 1000, "f32", 1.0, seq_lens=(1000, 637), seed=11),
+    si.custom("s1000_f32_u", 3, 2, 1000, "f32", 1.0, seq_len_range=(1, 1000), seed=12),
+    si.custom("s2048_bf16", 2, 2, 2048, "bf16", 0.125, seq_lens=(2048, 1500), x_std=2.0, seed=13),
+    si.custom("s4096_bf16", 2, 1, 4096, "bf16", 0.125, seq_lens=(4096, 3001), x_std=2.0, seed=14),
+    si.custom("s8192_f16", 1, 2, 8192, "f16", 0.125, seq_lens=(8192,), spike_prob=0.01, seed=15),
+    si.custom("s8192_f32", 1, 1, 8192, "f32", 1.0, seq_lens=(6001,), seed=16),
+    si.custom("s8192_bf16", 1, 1, 8192, "bf16", 0.125, seq_lens=(8192,), x_std=2.0, seed=17),
+]
+
+
+@pytest.mark.parametrize("w", REDUCED, ids=[w.name for w in REDUCED])
+def test_reduced_workloads(dev, w):
+    run_and_check(w, dev)
+
+
+EDGE_S = [1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 255, 256, 257,
+          511, 512, 513, 1000, 1023, 1024, 1025, 2047, 2048, 2049, 4095, 4096, 4097, 8191, 8192]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("S", EDGE_S)
+def test_edge_sizes(dev, S, dtype):
+    """Lengths -1 (clamped to 0), 0, 1, S//2+1 and S+3 (clamped to S) in one call."""
+    M = 2 if S <= 1024 else 1
+    w = si.custom(f"edge{S}", 5, M, S, dtype, 0.125 if dtype != "f32" else 1.0,
+                  seq_lens=(-1, 0, 1, S // 2 + 1, S + 3), x_std=2.0, seed=S)
+    run_and_check(w, dev)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("S", [5, 64, 1000, 2048, 8192])
+def test_element_aligned_buffers(dev, S, dtype):
+    """Buffers offset by one element: the element-granular path, same tolerances."""
+    w = si.custom(f"unaligned{S}", 2, 1, S, dtype, 0.5, seq_lens=(S, S // 3 + 1), seed=100 + S)
+    run_and_check(w, dev, offset_elems=1)
+
+
+def test_zero_length_batches_produce_all_zero_output(dev):
+    w = si.custom("zeros", 3, 2, 256, "f32", 1.0, seq_lens=(0, 0, 0), seed=3)
+    x = si.make_x(w, dev)
+    lens = _lens_dev(w, dev)
+    y = torch.full_like(x, float("nan"))
+    gtms.forward(x, lens, 1.0, out=y)
+    dx = torch.full_like(x, float("nan"))
+    gtms.backward(x, x, lens, 1.0, out=dx)
+    torch.cuda.synchronize()
+    assert bool((y.view(torch.int32) == 0).all()) and bool((dx.view(torch.int32) == 0).all())
+
+
+# ---------------------------------------------------------------------------
+# Properties: masked inputs are never read, every output is written, aliasing
+# ---------------------------------------------------------------------------
+
+def _kept_mask(lens, M, S, dev):
+    n = torch.from_numpy(oracle.kept_prefix_lengths(lens, M, S)).to(dev)        # [B, S]
+    col = torch.arange(S, device=dev)
+    return (col[None, None, :] < n[:, :, None])[:, None]                        # [B, 1, S, S]
+
+
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5), ("bf16", 33)])
+def test_masked_inputs_are_not_read(dev, dtype, S):
+    w = si.custom("sentinel", 3, 2, S, dtype, 0.125, seq_lens=(S, S // 2 + 1, 0), seed=21)
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    kept = _kept_mask(lens, w.M, S, dev)
+    x = si.make_x(w, dev)
+    dy = si.make_dy(w, dev)
+    y_ref = gtms.forward(x, lens_d, w.scale)
+    dx_ref = gtms.backward(y_ref, dy, lens_d, w.scale)
+    nan = torch.tensor(float("nan"), dtype=x.dtype, device=dev)
+    x_nan = torch.where(kept, x, nan)
+    y_in = torch.where(kept, y_ref, nan)
+    dy_nan = torch.where(kept, dy, nan)
+    y = gtms.forward(x_nan, lens_d, w.scale)
+    dx = gtms.backward(y_in, dy_nan, lens_d, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16 if dtype != "f32" else torch.int32),
+                       y_ref.view(torch.int16 if dtype != "f32" else torch.int32))
+    assert torch.equal(dx.view(torch.int16 if dtype != "f32" else torch.int32),
+                       dx_ref.view(torch.int16 if dtype != "f32" else torch.int32))
+
+
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 7)])
+def test_every_output_element_is_written(dev, dtype, S):
+    w = si.custom("prefill", 2, 2, S, dtype, 1.0, seq_lens=(S, S // 3), seed=22)
+    lens_d = _lens_dev(w, dev)
+    x = si.make_x(w, dev)
+    ref = gtms.forward(x, lens_d, 1.0)
+    y = torch.full_like(x, float("nan"))
+    gtms.forward(x, lens_d, 1.0, out=y)
+    dref = gtms.backward(ref, x, lens_d, 1.0)
+    dx = torch.full_like(x, float("nan"))
+    gtms.backward(ref, x, lens_d, 1.0, out=dx)
+    torch.cuda.synchronize()
+    assert not bool(torch.isnan(y).any()) and not bool(torch.isnan(dx).any())
+    assert torch.equal(y, ref) and torch.equal(dx, dref)
+    assert masked_bits_all_zero(y, lens_d, dtype) and masked_bits_all_zero(dx, lens_d, dtype)
+
+
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5)])
+def test_exact_aliasing_is_in_place(dev, dtype, S):
+    w = si.custom("alias", 2, 3, S, dtype, 0.125, seq_lens=(S, S // 2 + 3), seed=23)
+    lens_d = _lens_dev(w, dev)
+    x = si.make_x(w, dev)
+    dy = si.make_dy(w, dev)
+    y_ref = gtms.forward(x, lens_d, w.scale)
+    dx_ref = gtms.backward(y_ref, dy, lens_d, w.scale)
+    xi = x.clone()
+    gtms.forward(xi, lens_d, w.scale, out=xi)
+    dyi = dy.clone()
+    gtms.backward(y_ref, dyi, lens_d, w.scale, out=dyi)
+    yi = y_ref.clone()
+    gtms.backward(yi, dy, lens_d, w.scale, out=yi)
+    torch.cuda.synchronize()
+    assert torch.equal(xi, y_ref)
+    assert torch.equal(dyi, dx_ref)
+    assert torch.equal(yi, dx_ref)
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5)])
+def test_guard_bands_untouched(dev, dtype, S, offset):
+    """Canary bytes around each output stay intact (compute-sanitizer stand-in)."""
+    w = si.custom("guard", 2, 2, S, dtype, 1.0, seq_lens=(S, 1), seed=24)
+    lens_d = _lens_dev(w, dev)
+    x = si.make_x(w, dev)
+    n = x.numel()
+    pad = 4096 + offset
+    for direction in ("fwd", "bwd"):
+        buf = torch.full((n + 2 * pad,), -7.0, dtype=x.dtype, device=dev)
+        canary = buf.clone()
+        out = buf[pad:pad + n].view(x.shape)
+        if direction == "fwd":
+            gtms.forward(x, lens_d, 1.0, out=out)
+        else:
+            gtms.backward(x, x, lens_d, 1.0, out=out)
+        torch.cuda.synchronize()
+        assert torch.equal(buf[:pad], canary[:pad]) and torch.equal(buf[pad + n:], canary[pad + n:])
+
+
+def test_row0_is_exactly_one_hot(dev):
+    for dtype, S in (("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5)):
+        w = si.custom("row0", 3, 4, S, dtype, 0.37, seq_lens=(S, 1, 2), x_std=3.0, seed=25)
+        y = gtms.forward(si.make_x(w, dev), _lens_dev(w, dev), w.scale)
+        torch.cuda.synchronize()
+        assert bool((y[:, :, 0, 0].float() == 1.0).all())
+        assert bool((y[:, :, 0, 1:].float() == 0.0).all())
+
+
+def test_side_stream_and_determinism(dev):
+    w = si.custom("stream", 4, 8, 1000, "f32", 1.0, seq_len_range=(1, 1000), seed=26)
+    lens_d = _lens_dev(w, dev)
+    x = si.make_x(w, dev)
+    dy = si.make_dy(w, dev)
+    y0 = gtms.forward(x, lens_d)
+    d0 = gtms.backward(y0, dy, lens_d)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        y1 = gtms.forward(x, lens_d)
+        d1 = gtms.backward(y1, dy, lens_d)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1) and torch.equal(d0, d1)
+
+
+def test_autograd_function(dev):
+    w = si.custom("autograd", 2, 2, 64, "f32", 0.5, seq_lens=(64, 20), seed=27)
+    lens_d = _lens_dev(w, dev)
+    x = si.make_x(w, dev).requires_grad_(True)
+    dy = si.make_dy(w, dev)
+    y = gtms.grouped_tril_mask_softmax(x, lens_d, 0.5)
+    y.backward(dy)
+    torch.cuda.synchronize()
+    ref_y = gtms.forward(x.detach(), lens_d, 0.5)
+    ref_dx = gtms.backward(ref_y, dy, lens_d, 0.5)
+    assert torch.equal(y.detach(), ref_y) and torch.equal(x.grad, ref_dx)
+
+
+# ---------------------------------------------------------------------------
+# Full workload sizes, in the launch configuration the benchmark times
+# ---------------------------------------------------------------------------
+
+FULL = ["worked_example", "s1000_b3", "s1000_b12", "s2048_bf16", "s8192_f16", "s4096_bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(dev, name):
+    w = si.WORKLOADS[name]
+    B, M, S = w.B, w.M, w.S
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    x = si.make_x(w, dev)
+    y = gtms.forward(x, lens_d, w.scale)
+    torch.cuda.synchronize()
+    # every row: masked bits zero, live rows sum to 1
+    assert masked_bits_all_zero(y, lens_d, w.dtype)
+    tol = {"f32": 1e-5, "bf16": 2.0 ** -7, "f16": 2.0 ** -9}[w.dtype]
+    assert live_row_sums_close_to_one(y, lens_d, tol)
+    # sampled slices: element-wise against the oracle
+    slices = si.sample_slices(w, 6)
+    st = Stats()
+    for b, m in slices:
+        xs = to_bits(x[b, m], w.dtype).reshape(-1)
+        ys = to_bits(y[b, m], w.dtype).reshape(-1)
+        q_base = (b * M + m) * S
+        for a, e in row_chunks(0, S, S):
+            check_forward(xs[a * S:e * S], ys[a * S:e * S], lens, B, M, S, w.scale, w.dtype,
+                          q_base + a, q_base + e, st)
+    assert st.ok, f"forward {w.describe()}: {st}"
+    if not w.backward:
+        return
+    # backward: y input = GPU forward everywhere except the sampled slices,
+    # which hold the oracle's own forward (those are the slices compared).
+    dy = si.make_dy(w, dev)
+    y_in = y
+    for b, m in slices:
+        xs = to_bits(x[b, m], w.dtype).reshape(1, 1, S, S)
+        ref = oracle_forward_bits(xs, lens[b:b + 1], 1, 1, S, w.scale, w.dtype)
+        y_in[b, m].copy_(from_bits(ref, w.dtype, "cpu").view(S, S))
+    dx = gtms.backward(y_in, dy, lens_d, w.scale)
+    torch.cuda.synchronize()
+    assert masked_bits_all_zero(dx, lens_d, w.dtype)
+    assert bool(torch.isfinite(dx).all())
+    sb = Stats()
+    for b, m in slices:
+        ys = to_bits(y_in[b, m], w.dtype).reshape(-1)
+        gs = to_bits(dy[b, m], w.dtype).reshape(-1)
+        ds = to_bits(dx[b, m], w.dtype).reshape(-1)
+        q_base = (b * M + m) * S
+        for a, e in row_chunks(0, S, S):
+            check_backward(ys[a * S:e * S], gs[a * S:e * S], ds[a * S:e * S], lens, B, M, S, w.scale, w.dtype,
+                           q_base + a, q_base + e, sb)
+    assert sb.ok, f"backward {w.describe()}: {sb}"
+    del x, y, dy, dx, y_in
+    torch.cuda.empty_cache()
