@@ -383,42 +383,31 @@ def run_gpu(args, w, lens, rank, world, local_rank):
 
 
 def run_e2e(args, w, lens, dev, stream, fwd_c, bwd_c):
-    """Same step through the public API with the inputs in pinned host memory:
-    H2D of x, dy, seq_lens and D2H of y, dx inside the timed region."""
+    """Same step through the public host-buffer API: inputs in pinned host
+    memory, H2D of x, dy, seq_lens and D2H of y, dx inside the timed region
+    (chunks of batches pipelined over three streams)."""
     import torch
 
-    host = {}
+    import seeded_inputs as si
+    from masked_softmax_attention_gb300.pipeline import HostPipeline
+
     try:
         x_h = torch.empty((w.B, w.M, w.S, w.S), dtype=w.torch_dtype, pin_memory=True)
-        dy_h = torch.empty_like(x_h, pin_memory=True)
         y_h = torch.empty_like(x_h, pin_memory=True)
+        dy_h = torch.empty_like(x_h, pin_memory=True) if w.backward else None
         dx_h = torch.empty_like(x_h, pin_memory=True) if w.backward else None
     except RuntimeError as exc:
         return {"error": f"pinned host buffers unavailable: {exc}"}
-    import seeded_inputs as si
-
     x_h.copy_(si.make_x(w, dev))
-    dy_h.copy_(si.make_dy(w, dev))
+    if w.backward:
+        dy_h.copy_(si.make_dy(w, dev))
     lens_h = torch.from_numpy(lens).pin_memory()
-    x_d, dy_d = torch.empty_like(x_h, device=dev), torch.empty_like(x_h, device=dev)
-    y_d, dx_d = torch.empty_like(x_h, device=dev), torch.empty_like(x_h, device=dev)
-    lens_d = torch.empty_like(lens_h, device=dev)
-    B, M, S, code, scale, sp = w.B, w.M, w.S, w.dtype_code, float(w.scale), stream.cuda_stream
+    torch.cuda.empty_cache()
+    pipe = HostPipeline(w.B, w.M, w.S, w.torch_dtype, dev, chunk_batches=args.e2e_chunk, depth=2,
+                        backward=w.backward)
 
     def step():
-        x_d.copy_(x_h, non_blocking=True)
-        lens_d.copy_(lens_h, non_blocking=True)
-        if w.backward:
-            dy_d.copy_(dy_h, non_blocking=True)
-        rc = fwd_c(x_d.data_ptr(), y_d.data_ptr(), lens_d.data_ptr(), B, M, S, scale, code, sp)
-        if w.backward:
-            rc |= bwd_c(y_d.data_ptr(), dy_d.data_ptr(), dx_d.data_ptr(), lens_d.data_ptr(), B, M, S, scale,
-                        code, sp)
-        y_h.copy_(y_d, non_blocking=True)
-        if w.backward:
-            dx_h.copy_(dx_d, non_blocking=True)
-        if rc:
-            raise RuntimeError("libgtms call failed in the end-to-end loop")
+        pipe.run(x_h, lens_h, w.scale, y_h, dy_h, dx_h)
 
     step()
     torch.cuda.synchronize()
@@ -430,13 +419,11 @@ def run_e2e(args, w, lens, dev, stream, fwd_c, bwd_c):
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / args.e2e_steps
     fb, bb = required_bytes(w, lens)
-    tb = x_h.numel() * x_h.element_size()
-    h2d = tb * (2 if w.backward else 1) + lens_h.numel() * 4
-    d2h = tb * (2 if w.backward else 1)
-    del host
+    h2d, d2h = pipe.bytes_per_call()
     return {"value": round((fb + bb) / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "host_buffers": "pinned"}
+            "host_buffers": "pinned", "pipeline": f"{args.e2e_chunk} batch(es) per chunk, double-buffered, "
+                                                  "3 streams (copy-in, kernels, copy-out)"}
 
 
 def main():
@@ -447,6 +434,7 @@ def main():
     ap.add_argument("--impl", choices=["gtms", "reference"], default="gtms")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunk", type=int, default=1, help="batches per chunk in the host pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
