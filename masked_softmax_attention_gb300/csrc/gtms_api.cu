@@ -88,9 +88,9 @@ bool bad_alias(const void* out, const void* in, uint64_t bytes)
     return out != in && overlaps(out, bytes, in, bytes);
 }
 
-gtms::Geom make_geom(int64_t rows, int64_t M, int64_t S, int variant, int e)
+gtms::Geom make_geom(int direction, int64_t rows, int64_t M, int64_t S, int variant, int e)
 {
-    const gtms::Variant& v = gtms::variant_at(variant);
+    const gtms::Variant v = gtms::variant_at(direction, e, variant);
     gtms::Geom g;
     g.rows = rows;
     g.rows_per_b = M * S;
@@ -123,10 +123,10 @@ GTMS_EXPORT int gtms_forward(const void* x, void* y, const int32_t* seq_lens, in
         return GTMS_ERR_INVALID_ARG;
 
     const bool a16 = aligned_to(x, 16) && aligned_to(y, 16);
-    const int variant = gtms::pick_variant(S, e, a16);
+    const int variant = gtms::pick_variant(0, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
-    const gtms::Geom g = make_geom(c.rows, M, S, variant, e);
+    const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
     case GTMS_F32: gtms::launch_forward<float>(variant, x, y, seq_lens, g, scale, st); break;
@@ -152,10 +152,10 @@ GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int
         return GTMS_ERR_INVALID_ARG;
 
     const bool a16 = aligned_to(y, 16) && aligned_to(dy, 16) && aligned_to(dx, 16);
-    const int variant = gtms::pick_variant(S, e, a16);
+    const int variant = gtms::pick_variant(1, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
-    const gtms::Geom g = make_geom(c.rows, M, S, variant, e);
+    const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
     case GTMS_F32: gtms::launch_backward<float>(variant, y, dy, dx, seq_lens, g, scale, st); break;
@@ -181,26 +181,34 @@ GTMS_EXPORT int gtms_version(void) { return GTMS_VERSION; }
 GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16)
 {
     static const char* const kDtype[3] = {"f32", "bf16", "f16"};
-    constexpr int kVariants = gtms::kNumVec + gtms::kNumElem;
-    // [direction][dtype][variant], filled once (thread-safe static initialisation).
+    constexpr int kMaxRows = 16;
+    // [direction][dtype][vector rows, then element rows], filled once (thread-safe static init).
     struct Names {
-        char text[2][3][kVariants][64];
+        char text[2][3][2 * kMaxRows][72];
         Names()
         {
             for (int d = 0; d < 2; ++d)
-                for (int t = 0; t < 3; ++t)
-                    for (int v = 0; v < kVariants; ++v) {
-                        const gtms::Variant& var = gtms::variant_at(v);
-                        std::snprintf(text[d][t][v], sizeof text[d][t][v], "gtms_%s_kernel<%s,%s,team%d,x%d>",
-                                      d == 0 ? "fwd" : "bwd", kDtype[t], var.vec16 ? "vec16" : "elem", var.team,
-                                      var.per_thread);
-                    }
+                for (int t = 0; t < 3; ++t) {
+                    const int e = t == 0 ? 4 : 2;
+                    const gtms::VariantTable vt = gtms::vec_table(d, e);
+                    for (int i = 0; i < vt.count && i < kMaxRows; ++i)
+                        std::snprintf(text[d][t][i], sizeof text[d][t][i], "gtms_%s_vec_kernel<%s,team%d,x%d,minb%d>",
+                                      d == 0 ? "fwd" : "bwd", kDtype[t], vt.rows[i].team, vt.rows[i].per_thread,
+                                      vt.rows[i].min_ctas);
+                    for (int i = 0; i < gtms::count_of(gtms::kElem) && i < kMaxRows; ++i)
+                        std::snprintf(text[d][t][kMaxRows + i], sizeof text[d][t][kMaxRows + i],
+                                      "gtms_%s_elem_kernel<%s,team%d,x%d>", d == 0 ? "fwd" : "bwd", kDtype[t],
+                                      gtms::kElem[i].team, gtms::kElem[i].per_thread);
+                }
         }
     };
     static const Names names;
     const int e = elem_bytes(dtype);
     if ((direction != 0 && direction != 1) || e == 0 || S < 1 || S > GTMS_MAX_S)
         return "none";
-    const int v = gtms::pick_variant(S, e, aligned16 != 0);
-    return v < 0 ? "none" : names.text[direction][dtype][v];
+    const int v = gtms::pick_variant(direction, S, e, aligned16 != 0);
+    if (v < 0)
+        return "none";
+    return v >= gtms::kElemBase ? names.text[direction][dtype][kMaxRows + v - gtms::kElemBase]
+                                : names.text[direction][dtype][v];
 }

@@ -1,66 +1,96 @@
-// gtms_dispatch.h -- host-side choice of kernel variant (team size, units per
-// thread, 16-byte or element access) for a row length and dtype.
+// gtms_dispatch.h -- host-side choice of kernel variant for a row length, dtype
+// and direction.
+//
+// Vector variants (16-byte units; the row's byte length is a multiple of 16 and
+// every buffer is 16-byte aligned) are listed per direction and element size,
+// smallest row capacity first. The forward holds up to 16 (fp32) or 32 (16-bit)
+// kept elements per thread as fp32 exponentials; the backward holds up to 8
+// raw 16-byte units of y and of dy per thread. Rows too long for one warp take a
+// CTA of 64..512 threads. The last number is the minimum number of CTAs per SM
+// requested from the compiler (__launch_bounds__): it caps registers so that
+// enough rows are in flight per SM. These choices come from a sweep on GB300 of
+// team size, units per thread, register cap and grid shape over the
+// S = 1000 / 2048 / 4096 / 8192 workloads.
+//
+// Element variants (one element per unit) serve rows that are not 16-byte
+// multiples, and element-aligned buffers.
 #pragma once
 
 #include <cstdint>
 
+//                       id  team  units/thread  min CTAs/SM (0: no register cap)
+#define GTMS_FWD_VEC4(X) X(0, 32, 1, 8) X(1, 32, 2, 8) X(2, 32, 4, 8) X(3, 64, 4, 0) \
+                         X(4, 128, 4, 0) X(5, 256, 4, 0) X(6, 512, 4, 0)
+#define GTMS_FWD_VEC2(X) X(0, 32, 1, 8) X(1, 32, 2, 8) X(2, 32, 4, 6) X(3, 64, 4, 16) \
+                         X(4, 128, 4, 8) X(5, 256, 4, 4)
+#define GTMS_BWD_VEC4(X) X(0, 32, 1, 4) X(1, 32, 2, 4) X(2, 32, 4, 4) X(3, 32, 8, 5) \
+                         X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0)
+#define GTMS_BWD_VEC2(X) X(0, 32, 1, 4) X(1, 32, 2, 4) X(2, 32, 4, 4) X(3, 32, 8, 5) \
+                         X(4, 64, 8, 0) X(5, 128, 8, 0)
+//                       id  team  elements/thread
+#define GTMS_ELEM(X) X(0, 32, 1) X(1, 32, 4) X(2, 32, 16) X(3, 32, 32) X(4, 128, 32) X(5, 256, 32)
+
 namespace gtms {
 
 struct Variant {
-    int team;          // threads per row: 32 = one warp, otherwise the whole CTA
-    int per_thread;    // access units held per thread
-    bool vec16;        // 16-byte vector units (else one element per unit)
-    int max_units;     // team * per_thread
+    int team;         // threads per row: 32 = one warp, otherwise the whole CTA
+    int per_thread;   // access units held per thread
+    int min_ctas;     // __launch_bounds__ minimum CTAs per SM (0: none)
+    bool vec16;       // 16-byte units (else one element per unit)
+    int max_units;    // team * per_thread
 };
 
-// 16-byte vectors: every row starts on a 16-byte boundary and all buffers are
-// 16-byte aligned. Row capacity in vectors, smallest first.
-constexpr Variant kVecVariants[] = {
-    {32, 1, true, 32},      // rows <= 512 B
-    {32, 2, true, 64},      // <= 1 KB
-    {32, 4, true, 128},     // <= 2 KB
-    {32, 8, true, 256},     // <= 4 KB   (fp32 S = 1000, bf16 S = 2048)
-    {128, 4, true, 512},    // <= 8 KB
-    {256, 4, true, 1024},   // <= 16 KB  (fp16 / bf16 S = 8192)
-    {512, 4, true, 2048},   // <= 32 KB  (fp32 S = 8192)
+#define GTMS_VEC_ROW(id, tw, nv, mb) {tw, nv, mb, true, (tw) * (nv)},
+#define GTMS_ELEM_ROW(id, tw, nv) {tw, nv, 0, false, (tw) * (nv)},
+constexpr Variant kFwdVec4[] = {GTMS_FWD_VEC4(GTMS_VEC_ROW)};
+constexpr Variant kFwdVec2[] = {GTMS_FWD_VEC2(GTMS_VEC_ROW)};
+constexpr Variant kBwdVec4[] = {GTMS_BWD_VEC4(GTMS_VEC_ROW)};
+constexpr Variant kBwdVec2[] = {GTMS_BWD_VEC2(GTMS_VEC_ROW)};
+constexpr Variant kElem[] = {GTMS_ELEM(GTMS_ELEM_ROW)};
+#undef GTMS_VEC_ROW
+#undef GTMS_ELEM_ROW
+
+template <typename V, int N>
+constexpr int count_of(const V (&)[N]) { return N; }
+
+constexpr int kElemBase = 100;   // variant ids >= kElemBase are element variants
+
+struct VariantTable {
+    const Variant* rows;
+    int count;
 };
 
-// Element units: rows whose byte length is not a multiple of 16, or buffers
-// that are only element-aligned.
-constexpr Variant kElemVariants[] = {
-    {32, 1, false, 32},
-    {32, 4, false, 128},
-    {32, 16, false, 512},
-    {32, 32, false, 1024},
-    {128, 32, false, 4096},
-    {256, 32, false, 8192},
-};
+inline VariantTable vec_table(int direction, int elem_bytes)
+{
+    if (direction == 0)
+        return elem_bytes == 4 ? VariantTable{kFwdVec4, count_of(kFwdVec4)} : VariantTable{kFwdVec2, count_of(kFwdVec2)};
+    return elem_bytes == 4 ? VariantTable{kBwdVec4, count_of(kBwdVec4)} : VariantTable{kBwdVec2, count_of(kBwdVec2)};
+}
 
-constexpr int kNumVec = sizeof(kVecVariants) / sizeof(kVecVariants[0]);
-constexpr int kNumElem = sizeof(kElemVariants) / sizeof(kElemVariants[0]);
-
-// Index into kVecVariants (0..kNumVec-1) or kElemVariants (kNumVec..), or -1.
-inline int pick_variant(int64_t S, int elem_bytes, bool aligned16)
+// Variant id for (direction, S, element size, all buffers 16-byte aligned), or -1.
+inline int pick_variant(int direction, int64_t S, int elem_bytes, bool aligned16)
 {
     if (S <= 0)
         return -1;
-    const bool vec = aligned16 && ((S * elem_bytes) % 16 == 0);
-    if (vec) {
+    if (aligned16 && (S * elem_bytes) % 16 == 0) {
         const int64_t units = S * elem_bytes / 16;
-        for (int i = 0; i < kNumVec; ++i)
-            if (units <= kVecVariants[i].max_units)
+        const VariantTable t = vec_table(direction, elem_bytes);
+        for (int i = 0; i < t.count; ++i)
+            if (units <= t.rows[i].max_units)
                 return i;
         return -1;
     }
-    for (int i = 0; i < kNumElem; ++i)
-        if (S <= kElemVariants[i].max_units)
-            return kNumVec + i;
+    for (int i = 0; i < count_of(kElem); ++i)
+        if (S <= kElem[i].max_units)
+            return kElemBase + i;
     return -1;
 }
 
-inline const Variant& variant_at(int idx)
+inline Variant variant_at(int direction, int elem_bytes, int id)
 {
-    return idx < kNumVec ? kVecVariants[idx] : kElemVariants[idx - kNumVec];
+    if (id >= kElemBase)
+        return kElem[id - kElemBase];
+    return vec_table(direction, elem_bytes).rows[id];
 }
 
 }  // namespace gtms

@@ -76,16 +76,18 @@ def test_version_and_status_strings(lib):
 
 
 def test_kernel_choice(lib):
-    # warp per row for rows up to 4 KB of 16-byte vectors, a CTA per row beyond
-    assert gtms.kernel_name(0, 1000, F32) == "gtms_fwd_kernel<f32,vec16,team32,x8>"
-    assert gtms.kernel_name(1, 1000, F32) == "gtms_bwd_kernel<f32,vec16,team32,x8>"
-    assert gtms.kernel_name(0, 2048, BF16) == "gtms_fwd_kernel<bf16,vec16,team32,x8>"
-    assert gtms.kernel_name(1, 8192, F16) == "gtms_bwd_kernel<f16,vec16,team256,x4>"
-    assert gtms.kernel_name(0, 8192, F32) == "gtms_fwd_kernel<f32,vec16,team512,x4>"
-    # rows whose byte length is not a multiple of 16, or unaligned buffers: element access
-    assert gtms.kernel_name(0, 5, F32) == "gtms_fwd_kernel<f32,elem,team32,x1>"
-    assert gtms.kernel_name(0, 1000, F32, aligned16=False) == "gtms_fwd_kernel<f32,elem,team32,x32>"
-    assert gtms.kernel_name(0, 8191, F16) == "gtms_fwd_kernel<f16,elem,team256,x32>"
+    # vector kernels: a warp or a small CTA per row, sized by the row's 16-byte units
+    assert gtms.kernel_name(0, 1000, F32) == "gtms_fwd_vec_kernel<f32,team64,x4,minb0>"
+    assert gtms.kernel_name(1, 1000, F32) == "gtms_bwd_vec_kernel<f32,team32,x8,minb5>"
+    assert gtms.kernel_name(0, 2048, BF16) == "gtms_fwd_vec_kernel<bf16,team64,x4,minb16>"
+    assert gtms.kernel_name(1, 2048, BF16) == "gtms_bwd_vec_kernel<bf16,team32,x8,minb5>"
+    assert gtms.kernel_name(1, 8192, F16) == "gtms_bwd_vec_kernel<f16,team128,x8,minb0>"
+    assert gtms.kernel_name(0, 8192, F32) == "gtms_fwd_vec_kernel<f32,team512,x4,minb0>"
+    assert gtms.kernel_name(0, 1024, F16) == "gtms_fwd_vec_kernel<f16,team32,x4,minb6>"
+    # rows whose byte length is not a multiple of 16, or unaligned buffers: element kernels
+    assert gtms.kernel_name(0, 5, F32) == "gtms_fwd_elem_kernel<f32,team32,x1>"
+    assert gtms.kernel_name(0, 1000, F32, aligned16=False) == "gtms_fwd_elem_kernel<f32,team32,x32>"
+    assert gtms.kernel_name(1, 8191, F16) == "gtms_bwd_elem_kernel<f16,team256,x32>"
     # out of range
     assert gtms.kernel_name(0, 8193, F32) == "none"
     assert gtms.kernel_name(0, 0, F32) == "none"
