@@ -362,7 +362,10 @@ def run_gpu(args, w, lens, rank, world, local_rank):
                 "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'recipe fallback 6.8 TB/s'})",
                 "algorithmic_bytes_per_launch": dk["required_bytes"]}
 
-    e2e = run_e2e(args, wr, lens_r, dev, stream, fwd_c, bwd_c) if args.e2e_steps > 0 else None
+    e2e = e2e_staged = None
+    if args.e2e_steps > 0:
+        e2e = run_e2e_host_resident(args, wr, lens_r, dev, stream, fwd_c, bwd_c)
+        e2e_staged = run_e2e(args, wr, lens_r, dev, stream, fwd_c, bwd_c)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, lens)
@@ -374,12 +377,67 @@ def run_gpu(args, w, lens, rank, world, local_rank):
                 "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
                 "config": workload_config(w, lens), "pct_hbm_peak": round(100 * (value / world) / peak, 2),
-                "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_staged": e2e_staged,
                 "gpu_launches": K * (2 if wr.backward else 1), "clocks": clocks,
                 "impl": "gtms"}
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_e2e_host_resident(args, w, lens, dev, stream, fwd_c, bwd_c):
+    """The step through the C ABI with every tensor in pinned host memory: the
+    kernels read the kept inputs from, and write every output to, host memory
+    over the host link (gtms_device_pointer_of_host), no staging copy."""
+    import torch
+
+    import masked_softmax_attention_gb300 as gtms
+    import seeded_inputs as si
+
+    try:
+        x_h = torch.empty((w.B, w.M, w.S, w.S), dtype=w.torch_dtype, pin_memory=True)
+        y_h = torch.empty_like(x_h, pin_memory=True)
+        dy_h = torch.empty_like(x_h, pin_memory=True) if w.backward else None
+        dx_h = torch.empty_like(x_h, pin_memory=True) if w.backward else None
+    except RuntimeError as exc:
+        return {"error": f"pinned host buffers unavailable: {exc}"}
+    x_h.copy_(si.make_x(w, dev))
+    if w.backward:
+        dy_h.copy_(si.make_dy(w, dev))
+    lens_h = torch.from_numpy(lens).pin_memory()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    dp = gtms.device_pointer_of_host
+    xp, yp, lp = dp(x_h.data_ptr()), dp(y_h.data_ptr()), dp(lens_h.data_ptr())
+    dyp = dp(dy_h.data_ptr()) if w.backward else None
+    dxp = dp(dx_h.data_ptr()) if w.backward else None
+    B, M, S, code, scale, sp = w.B, w.M, w.S, w.dtype_code, float(w.scale), stream.cuda_stream
+
+    def step():
+        rc = fwd_c(xp, yp, lp, B, M, S, scale, code, sp)
+        if w.backward:
+            rc |= bwd_c(yp, dyp, dxp, lp, B, M, S, scale, code, sp)
+        if rc:
+            raise RuntimeError("libgtms call failed in the end-to-end loop")
+
+    step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / args.e2e_steps
+    fb, bb = required_bytes(w, lens)
+    dense = w.B * w.M * w.S * w.S * w.elem_bytes
+    kept = fb - dense                       # kept-prefix bytes of one tensor
+    h2d = kept + (2 * kept if w.backward else 0) + 4 * w.B
+    d2h = dense * (2 if w.backward else 1)
+    return {"value": round((fb + bb) / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "host_buffers": "pinned, mapped; kernels read kept x, y, dy from and write y, dx to host memory "
+                            "over NVLink-C2C (no staging copy)"}
 
 
 def run_e2e(args, w, lens, dev, stream, fwd_c, bwd_c):

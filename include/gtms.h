@@ -24,8 +24,9 @@
  * to nearest, ties to even.
  *
  * Ownership and threading. The caller owns every buffer. All tensor
- * pointers are DEVICE pointers on the current CUDA device; seq_lens is a
- * device int32[B]. The library allocates nothing, keeps no per-call state, is
+ * pointers are addresses the current CUDA device can dereference: device
+ * memory, or page-locked host memory mapped with gtms_device_pointer_of_host;
+ * seq_lens is an int32[B] array in such memory. The library allocates nothing, keeps no per-call state, is
  * safe to call from several host threads, and never synchronises: work is
  * enqueued on `stream` (a cudaStream_t passed as void*; NULL is the legacy
  * default stream) and the call returns at once. The host never reads
@@ -40,7 +41,10 @@
  *   GTMS_ERR_INVALID_ARG null pointer with B*M*S > 0, B/M/S < 0, a size whose
  *                        byte count overflows, a non-finite scale, a pointer
  *                        not aligned to its element size, partial overlap.
- *   GTMS_ERR_UNSUPPORTED unknown dtype, or S > GTMS_MAX_S.
+ *   GTMS_ERR_UNSUPPORTED unknown dtype; S > GTMS_MAX_S; or S > 8192 with a row
+ *                        whose byte length is not a multiple of 16 or a buffer
+ *                        that is not 16-byte aligned (long rows are split over a
+ *                        cluster of CTAs in 16-byte units only).
  *   GTMS_ERR_CUDA        the kernel launch failed (cudaGetLastError()).
  * All argument checks run on the host before anything is enqueued; a call
  * that returns an error has enqueued nothing.
@@ -55,7 +59,7 @@ extern "C" {
 #endif
 
 #define GTMS_VERSION 1
-#define GTMS_MAX_S 8192
+#define GTMS_MAX_S 65536
 
 typedef enum { GTMS_F32 = 0, GTMS_BF16 = 1, GTMS_F16 = 2 } gtms_dtype;
 
@@ -88,6 +92,20 @@ int gtms_forward(const void* x, void* y, const int32_t* seq_lens,
  */
 int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_lens,
                   int64_t B, int64_t M, int64_t S, float scale, int dtype, void* stream);
+
+/*
+ * Device address of a page-locked host buffer (allocated with cudaHostAlloc
+ * or registered with cudaHostRegister), for passing host-resident tensors
+ * straight to gtms_forward / gtms_backward: the kernels then read the kept
+ * inputs from, and write every output to, host memory over the host link
+ * (NVLink-C2C on Grace-Blackwell), with no staging copy.
+ *   host     pointer into a page-locked host allocation.
+ *   device   out: the address the current device uses for it.
+ * Returns GTMS_ERR_INVALID_ARG for null arguments or memory that is not
+ * page-locked and mapped, GTMS_ERR_CUDA for other runtime errors. Host-only,
+ * enqueues nothing, allocates nothing.
+ */
+int gtms_device_pointer_of_host(const void* host, void** device);
 
 /* Static, NUL-terminated name of a status code ("GTMS_OK", ...). */
 const char* gtms_status_string(int status);

@@ -23,10 +23,10 @@ from ._build import LIB_PATH, build_library  # noqa: F401  (re-exported for buil
 
 GTMS_F32, GTMS_BF16, GTMS_F16 = 0, 1, 2
 GTMS_OK, GTMS_ERR_INVALID_ARG, GTMS_ERR_UNSUPPORTED, GTMS_ERR_CUDA = 0, 1, 2, 3
-GTMS_MAX_S = 8192
+GTMS_MAX_S = 65536
 
 EXPORTED_SYMBOLS = ("gtms_forward", "gtms_backward", "gtms_status_string", "gtms_version",
-                    "gtms_kernel_name")
+                    "gtms_kernel_name", "gtms_device_pointer_of_host")
 
 _lib = None
 _lock = threading.Lock()
@@ -63,6 +63,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.gtms_version.restype = ctypes.c_int
         lib.gtms_kernel_name.argtypes = [ctypes.c_int, i64, ctypes.c_int, ctypes.c_int]
         lib.gtms_kernel_name.restype = ctypes.c_char_p
+        lib.gtms_device_pointer_of_host.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
+        lib.gtms_device_pointer_of_host.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -90,6 +92,15 @@ def gtms_version() -> int:
 
 def kernel_name(direction: int, S: int, dtype: int, aligned16: bool = True) -> str:
     return load_library().gtms_kernel_name(direction, S, dtype, 1 if aligned16 else 0).decode()
+
+
+def device_pointer_of_host(host_ptr: int) -> int:
+    """Device address of a page-locked host buffer (``gtms_device_pointer_of_host``)."""
+    out = ctypes.c_void_p()
+    rc = load_library().gtms_device_pointer_of_host(host_ptr, ctypes.byref(out))
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_device_pointer_of_host", rc)
+    return out.value
 
 
 # ---------------------------------------------------------------------------
@@ -156,6 +167,57 @@ def backward(y, dy, seq_lens, scale: float = 1.0, out=None):
     stream = torch.cuda.current_stream(y.device).cuda_stream
     rc = gtms_backward(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), seq_lens.data_ptr(), B, M, S,
                        float(scale), _dtype_code(y), stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_backward", rc)
+    return dx
+
+
+def _check_pinned(name, t):
+    if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous page-locked (pinned) CPU tensor")
+
+
+def forward_host(x, seq_lens, scale: float = 1.0, out=None, device=None):
+    """Forward on pinned host tensors: the kernels read x and write y in host memory.
+
+    ``x`` [B,M,S,S], ``seq_lens`` int32 [B] and ``out`` (allocated pinned if
+    omitted) stay in page-locked host memory; the call is enqueued on the
+    current stream of ``device`` and returns at once (synchronise before
+    reading ``out``).
+    """
+    import torch
+
+    _check_pinned("x", x)
+    _check_pinned("seq_lens", seq_lens)
+    if x.dim() != 4 or x.shape[-1] != x.shape[-2] or seq_lens.dtype != torch.int32 or seq_lens.shape != x.shape[:1]:
+        raise ValueError("x must be [B, M, S, S] and seq_lens int32 [B]")
+    y = torch.empty_like(x).pin_memory() if out is None else out
+    _check_pinned("out", y)
+    B, M, S, _ = x.shape
+    stream = torch.cuda.current_stream(device).cuda_stream
+    rc = gtms_forward(device_pointer_of_host(x.data_ptr()), device_pointer_of_host(y.data_ptr()),
+                      device_pointer_of_host(seq_lens.data_ptr()), B, M, S, float(scale), _dtype_code(x), stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_forward", rc)
+    return y
+
+
+def backward_host(y, dy, seq_lens, scale: float = 1.0, out=None, device=None):
+    """Backward on pinned host tensors (see ``forward_host``)."""
+    import torch
+
+    for name, t in (("y", y), ("dy", dy), ("seq_lens", seq_lens)):
+        _check_pinned(name, t)
+    if dy.shape != y.shape or dy.dtype != y.dtype or y.dim() != 4 or seq_lens.dtype != torch.int32 \
+            or seq_lens.shape != y.shape[:1]:
+        raise ValueError("y and dy must be matching [B, M, S, S] tensors and seq_lens int32 [B]")
+    dx = torch.empty_like(y).pin_memory() if out is None else out
+    _check_pinned("out", dx)
+    B, M, S, _ = y.shape
+    stream = torch.cuda.current_stream(device).cuda_stream
+    rc = gtms_backward(device_pointer_of_host(y.data_ptr()), device_pointer_of_host(dy.data_ptr()),
+                       device_pointer_of_host(dx.data_ptr()), device_pointer_of_host(seq_lens.data_ptr()),
+                       B, M, S, float(scale), _dtype_code(y), stream)
     if rc != GTMS_OK:
         raise GtmsError("gtms_backward", rc)
     return dx

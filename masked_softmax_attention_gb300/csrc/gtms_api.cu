@@ -165,6 +165,24 @@ GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int
     return launch_status();
 }
 
+GTMS_EXPORT int gtms_device_pointer_of_host(const void* host, void** device)
+{
+    if (!host || !device)
+        return GTMS_ERR_INVALID_ARG;
+    void* d = nullptr;
+    const cudaError_t e = cudaHostGetDevicePointer(&d, const_cast<void*>(host), 0);
+    if (e == cudaErrorInvalidValue) {
+        cudaGetLastError();
+        return GTMS_ERR_INVALID_ARG;
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GTMS_ERR_CUDA;
+    }
+    *device = d;
+    return GTMS_OK;
+}
+
 GTMS_EXPORT const char* gtms_status_string(int status)
 {
     switch (status) {
@@ -182,9 +200,9 @@ GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, in
 {
     static const char* const kDtype[3] = {"f32", "bf16", "f16"};
     constexpr int kMaxRows = 16;
-    // [direction][dtype][vector rows, then element rows], filled once (thread-safe static init).
+    // [direction][dtype][vector rows, element rows, cluster rows], filled once (thread-safe static init).
     struct Names {
-        char text[2][3][2 * kMaxRows][72];
+        char text[2][3][3 * kMaxRows][80];
         Names()
         {
             for (int d = 0; d < 2; ++d)
@@ -199,6 +217,12 @@ GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, in
                         std::snprintf(text[d][t][kMaxRows + i], sizeof text[d][t][kMaxRows + i],
                                       "gtms_%s_elem_kernel<%s,team%d,x%d>", d == 0 ? "fwd" : "bwd", kDtype[t],
                                       gtms::kElem[i].team, gtms::kElem[i].per_thread);
+                    const gtms::VariantTable ct = gtms::cluster_table(d, e);
+                    for (int i = 0; i < ct.count && i < kMaxRows; ++i)
+                        std::snprintf(text[d][t][2 * kMaxRows + i], sizeof text[d][t][2 * kMaxRows + i],
+                                      "gtms_%s_cluster_kernel<%s,cluster%d,team%d,x%d,minb%d>", d == 0 ? "fwd" : "bwd",
+                                      kDtype[t], ct.rows[i].cluster, ct.rows[i].team, ct.rows[i].per_thread,
+                                      ct.rows[i].min_ctas);
                 }
         }
     };
@@ -209,6 +233,8 @@ GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, in
     const int v = gtms::pick_variant(direction, S, e, aligned16 != 0);
     if (v < 0)
         return "none";
+    if (v >= gtms::kClusterBase)
+        return names.text[direction][dtype][2 * kMaxRows + v - gtms::kClusterBase];
     return v >= gtms::kElemBase ? names.text[direction][dtype][kMaxRows + v - gtms::kElemBase]
                                 : names.text[direction][dtype][v];
 }

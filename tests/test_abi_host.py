@@ -88,8 +88,14 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name(0, 5, F32) == "gtms_fwd_elem_kernel<f32,team32,x1>"
     assert gtms.kernel_name(0, 1000, F32, aligned16=False) == "gtms_fwd_elem_kernel<f32,team32,x32>"
     assert gtms.kernel_name(1, 8191, F16) == "gtms_bwd_elem_kernel<f16,team256,x32>"
+    # rows longer than one CTA holds: a cluster of CTAs per row, 16-byte units only
+    assert gtms.kernel_name(0, 16384, F32) == "gtms_fwd_cluster_kernel<f32,cluster2,team512,x4,minb0>"
+    assert gtms.kernel_name(1, 65536, BF16) == "gtms_bwd_cluster_kernel<bf16,cluster8,team128,x8,minb0>"
+    assert gtms.kernel_name(0, 8200, F16) == "gtms_fwd_cluster_kernel<f16,cluster2,team256,x4,minb0>"
+    assert gtms.kernel_name(0, 16384, F32, aligned16=False) == "none"
     # out of range
     assert gtms.kernel_name(0, 8193, F32) == "none"
+    assert gtms.kernel_name(0, 65537, BF16) == "none"
     assert gtms.kernel_name(0, 0, F32) == "none"
     assert gtms.kernel_name(2, 100, F32) == "none"
     assert gtms.kernel_name(0, 100, 7) == "none"
@@ -115,6 +121,13 @@ def test_shape_and_scale_errors(lib, call):
     assert call(S=gtms.GTMS_MAX_S + 1) == UNSUPPORTED
     # byte count overflows int64
     assert call(B=1 << 30, M=1 << 30, S=4096) == INVALID
+
+
+@pytest.mark.parametrize("call", [fwd, bwd])
+def test_long_rows_need_16_byte_units(lib, call):
+    assert call(S=8193) == UNSUPPORTED                  # fp32 row of 32772 bytes
+    assert call(S=8196, dtype=F16) == UNSUPPORTED       # 16392 bytes
+    assert call(S=65536 + 8) == UNSUPPORTED             # beyond GTMS_MAX_S
 
 
 @pytest.mark.parametrize("call", [fwd, bwd])
@@ -152,6 +165,13 @@ def test_backward_pointer_errors(lib):
     assert bwd(dx=X + nbytes - 4) == INVALID          # partial overlap with y
     assert bwd(lens=Y + 128) == INVALID               # seq_lens inside dx
     assert bwd(dy=DY + 1) == INVALID
+
+
+def test_device_pointer_of_host_rejects_bad_arguments(lib):
+    out = ctypes.c_void_p()
+    assert lib.gtms_device_pointer_of_host(None, ctypes.byref(out)) == INVALID
+    buf = ctypes.create_string_buffer(64)
+    assert lib.gtms_device_pointer_of_host(ctypes.addressof(buf), None) == INVALID
 
 
 def test_tensor_api_rejects_cpu_tensors(lib):

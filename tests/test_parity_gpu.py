@@ -339,3 +339,84 @@ def test_host_pipeline_matches_device_calls(dev, chunk):
         pipe.run(x_h, torch.from_numpy(lens).pin_memory(), 1.0, y_h, dy_h, dx_h)
         torch.cuda.current_stream().synchronize()
         assert torch.equal(y_h, y_ref.cpu()) and torch.equal(dx_h, dx_ref.cpu())
+
+
+# ---------------------------------------------------------------------------
+# Rows longer than one CTA holds (8192 < S <= 65536): a cluster of CTAs per row
+# ---------------------------------------------------------------------------
+
+LONG_FULL = [(8200, "f32"), (8200, "bf16"), (12288, "f16"), (16384, "f32"), (16384, "bf16")]
+
+
+@pytest.mark.parametrize("S,dtype", LONG_FULL)
+def test_long_rows_full_comparison(dev, S, dtype):
+    """Every element, lengths S, S//2+1, 1 and 0 (rows spread over 2 or 4 CTAs)."""
+    w = si.custom(f"long{S}", 4, 1, S, dtype, 0.125 if dtype != "f32" else 0.7,
+                  seq_lens=(S, S // 2 + 1, 1, 0), x_std=2.0, seed=S + 7)
+    run_and_check(w, dev)
+
+
+@pytest.mark.parametrize("S,dtype,L", [(32768, "f32", 20001), (32768, "bf16", 32768), (65536, "bf16", 40000),
+                                       (65536, "f16", 65536)])
+def test_long_rows_sampled(dev, S, dtype, L):
+    """Largest rows: sampled rows element by element, every row's masked bits and
+    live row sums on the device."""
+    w = si.custom(f"long{S}", 1, 1, S, dtype, 0.125, seq_lens=(L,), seed=S + L)
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    x = si.make_x(w, dev)
+    y = gtms.forward(x, lens_d, w.scale)
+    dy = si.make_dy(w, dev)
+    rng = np.random.default_rng(S)
+    rows = sorted({0, 1, 2, L - 1, L - 2, L // 2, L, S - 1} | set(rng.integers(0, L, 12).tolist()))
+    rows = [r for r in rows if 0 <= r < S]
+    # backward input: the oracle's own forward on the sampled rows, the GPU's elsewhere
+    y_in = y.clone()
+    for r in rows:
+        xs = to_bits(x[0, 0, r:r + 1], w.dtype).reshape(-1)
+        ref = oracle.forward(xs, lens, 1, 1, S, w.scale, w.dtype_code, r, r + 1)
+        y_in[0, 0, r].copy_(from_bits(oracle.round_to(ref, w.dtype_code), w.dtype, "cpu").view(S))
+    dx = gtms.backward(y_in, dy, lens_d, w.scale)
+    torch.cuda.synchronize()
+    assert masked_bits_all_zero(y, lens_d, w.dtype) and masked_bits_all_zero(dx, lens_d, w.dtype)
+    tol = {"f32": 1e-5, "bf16": 2.0 ** -7, "f16": 2.0 ** -9}[w.dtype]
+    assert live_row_sums_close_to_one(y, lens_d, tol)
+    st, sb = Stats(), Stats()
+    for r in rows:
+        check_forward(to_bits(x[0, 0, r:r + 1], w.dtype).reshape(-1), to_bits(y[0, 0, r:r + 1], w.dtype).reshape(-1),
+                      lens, 1, 1, S, w.scale, w.dtype, r, r + 1, st)
+        check_backward(to_bits(y_in[0, 0, r:r + 1], w.dtype).reshape(-1), to_bits(dy[0, 0, r:r + 1], w.dtype).reshape(-1),
+                       to_bits(dx[0, 0, r:r + 1], w.dtype).reshape(-1), lens, 1, 1, S, w.scale, w.dtype, r, r + 1, sb)
+    assert st.ok, f"forward {w.describe()}: {st}"
+    assert sb.ok, f"backward {w.describe()}: {sb}"
+    del x, y, dy, dx, y_in
+    torch.cuda.empty_cache()
+
+
+def test_long_rows_that_are_not_16_byte_multiples_are_rejected(dev):
+    lens = torch.ones(1, dtype=torch.int32, device=dev)
+    x = torch.zeros(1, 1, 8196, 8196, dtype=torch.float16, device=dev)
+    with pytest.raises(gtms.GtmsError, match="UNSUPPORTED"):
+        gtms.forward(x, lens)
+    with pytest.raises(gtms.GtmsError, match="UNSUPPORTED"):
+        gtms.backward(x, x, lens)
+
+
+def test_host_resident_buffers_match_device_calls(dev):
+    """Pinned host tensors passed straight to the kernels (no staging copy) give
+    the same bits as device-resident tensors."""
+    w = si.custom("hostres", 3, 4, 1000, "f32", 1.0, seq_len_range=(1, 1000), seed=41)
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    x = si.make_x(w, dev)
+    dy = si.make_dy(w, dev)
+    y_ref = gtms.forward(x, lens_d, 1.0)
+    dx_ref = gtms.backward(y_ref, dy, lens_d, 1.0)
+    x_h, dy_h = x.cpu().pin_memory(), dy.cpu().pin_memory()
+    lens_h = torch.from_numpy(lens).pin_memory()
+    y_h = gtms.forward_host(x_h, lens_h, 1.0, device=dev)
+    dx_h = gtms.backward_host(y_h, dy_h, lens_h, 1.0, device=dev)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h, y_ref.cpu()) and torch.equal(dx_h, dx_ref.cpu())
+    with pytest.raises(gtms.GtmsError, match="INVALID_ARG"):
+        gtms.device_pointer_of_host(torch.zeros(16).data_ptr())   # pageable, not page-locked
