@@ -254,6 +254,45 @@ def run_reference(args, w, lens):
 
 
 # ---------------------------------------------------------------------------
+# Multi-rank logic (one process per GPU; rows are independent, so each rank
+# runs its own replica of the workload and only the step time is reduced)
+# ---------------------------------------------------------------------------
+
+def replica_workload(w, rank):
+    """Rank r's replica: same shape and distribution, seed offset by rank."""
+    import dataclasses
+
+    return w if rank == 0 else dataclasses.replace(w, seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(value, dist, device):
+    """Largest per-rank value (the step time of the slowest rank)."""
+    import torch
+
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, dist, device):
+    """Total over ranks (each rank's replica has its own seeded lengths, so its own byte count)."""
+    import torch
+
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def whole_job_gbs(total_bytes, ms_step):
+    """Bytes moved by all ranks in one step over the slowest rank's step time."""
+    return total_bytes / (ms_step * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
@@ -283,8 +322,7 @@ def run_gpu(args, w, lens, rank, world, local_rank):
 
         dist.init_process_group("nccl", device_id=dev)
 
-    # per-rank replica: same shape, seed offset by rank
-    wr = si.Workload(**{**w.__dict__, "seed": w.seed + 1000 * rank}) if rank else w
+    wr = replica_workload(w, rank)
     lens_r = si.seq_lens(wr)
     x = si.make_x(wr, dev)
     dy = si.make_dy(wr, dev)
@@ -334,16 +372,11 @@ def run_gpu(args, w, lens, rank, world, local_rank):
     total_ms = start.elapsed_time(end)
     fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev) if wr.backward else 0.0
-    ms_step = total_ms / K
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / K, dist, dev)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
 
     fb, bb = required_bytes(wr, lens_r)
-    step_bytes = fb + bb
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(sum_over_ranks(fb + bb, dist, dev), ms_step)
 
     peak, peak_kind = hbm_peak()
     kern = {}

@@ -101,8 +101,11 @@ int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_le
  * (NVLink-C2C on Grace-Blackwell), with no staging copy.
  *   host     pointer into a page-locked host allocation.
  *   device   out: the address the current device uses for it.
- * Returns GTMS_ERR_INVALID_ARG for null arguments or memory that is not
- * page-locked and mapped, GTMS_ERR_CUDA for other runtime errors. Host-only,
+ * Returns GTMS_ERR_INVALID_ARG for null arguments or for memory the CUDA
+ * runtime cannot map for the current device, GTMS_ERR_CUDA for other runtime
+ * errors. (Where the device reads pageable host memory through the host's page
+ * tables, as on Grace-Blackwell, the runtime maps pageable memory as well;
+ * page-locked memory is still what the transfer rate assumes.) Host-only,
  * enqueues nothing, allocates nothing.
  */
 int gtms_device_pointer_of_host(const void* host, void** device);

@@ -60,6 +60,11 @@ def _load():
             i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
             lib.gtms_oracle_forward.argtypes = [vp, ctypes.c_int, vp, i64, i64, i64, dp, i64, i64, vp]
             lib.gtms_oracle_backward.argtypes = [vp, vp, ctypes.c_int, vp, i64, i64, i64, dp, i64, i64, vp]
+            ci = ctypes.c_int
+            lib.gtms_oracle_forward_masked.argtypes = [vp, ci, vp, i64, i64, i64, dp, ci, i64, i64, i64, vp]
+            lib.gtms_oracle_backward_masked.argtypes = [vp, vp, ci, vp, i64, i64, i64, dp, ci, i64, i64, i64, vp]
+            lib.gtms_oracle_forward_masked.restype = ctypes.c_int
+            lib.gtms_oracle_backward_masked.restype = ctypes.c_int
             lib.gtms_oracle_round.argtypes = [vp, i64, ctypes.c_int, vp]
             lib.gtms_oracle_decode.argtypes = [vp, i64, ctypes.c_int, vp]
             for f in (lib.gtms_oracle_forward, lib.gtms_oracle_backward,
@@ -85,7 +90,7 @@ def _row_chunks(row_begin: int, row_end: int, threads: int):
     return [(r, min(r + step, row_end)) for r in range(row_begin, row_end, step)]
 
 
-def _run_rows(kernel, ins, dtype, seq_lens, B, M, S, scale, row_begin, row_end, threads):
+def _run_rows(kernel, ins, dtype, seq_lens, B, M, S, scale, row_begin, row_end, threads, mask=None):
     lib = _load()
     seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
     if seq.shape != (B,):
@@ -102,7 +107,8 @@ def _run_rows(kernel, ins, dtype, seq_lens, B, M, S, scale, row_begin, row_end, 
         r0, r1 = chunk
         off = (r0 - row_begin) * S
         ptrs = [ctypes.c_void_p(a.ctypes.data + off * eb) for a in arrs]
-        rc = getattr(lib, kernel)(*ptrs, dtype, seq.ctypes.data, B, M, S, float(scale), r0, r1,
+        extra = () if mask is None else (int(mask[0]), int(mask[1]))
+        rc = getattr(lib, kernel)(*ptrs, dtype, seq.ctypes.data, B, M, S, float(scale), *extra, r0, r1,
                                   ctypes.c_void_p(out.ctypes.data + off * 8))
         if rc != 0:
             raise ValueError(f"{kernel} rejected its arguments")
@@ -116,22 +122,28 @@ def _run_rows(kernel, ins, dtype, seq_lens, B, M, S, scale, row_begin, row_end, 
     return out
 
 
-def forward(x, seq_lens, B, M, S, scale, dtype, row_begin=0, row_end=None, threads=1):
+MASK_GROUPED_TRIL, MASK_LENGTH, MASK_SLIDING_WINDOW = 0, 1, 2
+
+
+def forward(x, seq_lens, B, M, S, scale, dtype, row_begin=0, row_end=None, threads=1, mask_kind=0, window=0):
     """Masked softmax of rows [row_begin, row_end) of X[B,M,S,S] in double.
 
     ``x`` holds exactly those rows (raw element bits for bf16/fp16, uint32 bits
     or float32 values for fp32, float64 for F64). Returns float64 [rows, S].
+    ``mask_kind``: 0 grouped tril (default), 1 length mask, 2 sliding causal
+    window of width ``window`` (see gtms_oracle.c).
     """
     row_end = B * M * S if row_end is None else row_end
-    return _run_rows("gtms_oracle_forward", [x], dtype, seq_lens, B, M, S, scale,
-                     row_begin, row_end, threads)
+    return _run_rows("gtms_oracle_forward_masked", [x], dtype, seq_lens, B, M, S, scale,
+                     row_begin, row_end, threads, mask=(mask_kind, window))
 
 
-def backward(y, dy, seq_lens, B, M, S, scale, dtype, row_begin=0, row_end=None, threads=1):
+def backward(y, dy, seq_lens, B, M, S, scale, dtype, row_begin=0, row_end=None, threads=1, mask_kind=0,
+             window=0):
     """Softmax backward dx = scale*y*(dy - rowsum(dy*y)) under the same mask, in double."""
     row_end = B * M * S if row_end is None else row_end
-    return _run_rows("gtms_oracle_backward", [y, dy], dtype, seq_lens, B, M, S, scale,
-                     row_begin, row_end, threads)
+    return _run_rows("gtms_oracle_backward_masked", [y, dy], dtype, seq_lens, B, M, S, scale,
+                     row_begin, row_end, threads, mask=(mask_kind, window))
 
 
 def round_to(values, dtype: int) -> np.ndarray:
@@ -162,3 +174,17 @@ def kept_prefix_lengths(seq_lens, M: int, S: int) -> np.ndarray:
     L = np.clip(np.asarray(seq_lens, dtype=np.int64), 0, S)[:, None]
     r = np.arange(S, dtype=np.int64)[None, :]
     return np.where(r < L, r + 1, 0)
+
+
+def kept_ranges(seq_lens, S: int, mask_kind: int = 0, window: int = 0):
+    """(c0, c1) per (b, r), each [B, S]: the kept column range of every mask family."""
+    L = np.clip(np.asarray(seq_lens, dtype=np.int64), 0, S)[:, None]
+    r = np.arange(S, dtype=np.int64)[None, :]
+    live = r < L
+    if mask_kind == 1:
+        c1 = np.where(live, L, 0)
+        c0 = np.zeros_like(c1)
+    else:
+        c1 = np.where(live, r + 1, 0)
+        c0 = np.where(live, np.maximum(r - window + 1, 0), 0) if mask_kind == 2 else np.zeros_like(c1)
+    return c0, c1

@@ -35,6 +35,17 @@
  * seq_len values outside [0, S] are clamped to that range (reading taken: the
  * pages only show 1 <= seq_len <= S).
  *
+ * Mask families ("优化ScaledMaskSoftmax算子", section 6, lists a local window
+ * mask and a length mask besides the default). Every family keeps a
+ * contiguous column range [c0, c1) of row r < L and nothing of rows r >= L:
+ *   kind 0, grouped tril (default): [0, r + 1);
+ *   kind 1, length mask:            [0, L)          (key padding; r < L only);
+ *   kind 2, sliding causal window:  [max(0, r - w + 1), r + 1), window w >= 1.
+ * Reading taken for kind 2: the section's garbled tril(window_size) snippet
+ * under the heading "local window attention" is read as the usual causal band
+ * of width w. Reading taken for kind 1: padded query rows stay all-zero, as in
+ * the default op.
+ *
  * Build: cc -O2 -fno-fast-math -fPIC -shared gtms_oracle.c -o libgtms_oracle.so -lm
  */
 #include <math.h>
@@ -171,8 +182,10 @@ static void store_rounded(void* out, int64_t i, double v, int dtype)
 
 /* ---- mask ---- */
 
-/* Number of kept columns of row q (flat row id over [B, M, S]). */
-static int64_t kept_prefix(const int32_t* seq_lens, int64_t M, int64_t S, int64_t q)
+/* Kept column range [*c0, *c1) of row q (flat row id over [B, M, S]); empty
+ * when *c1 <= *c0. */
+static void kept_range(const int32_t* seq_lens, int64_t M, int64_t S, int kind, int64_t window, int64_t q,
+                       int64_t* c0, int64_t* c1)
 {
     const int64_t b = q / (M * S);
     const int64_t r = q % S;
@@ -181,7 +194,17 @@ static int64_t kept_prefix(const int32_t* seq_lens, int64_t M, int64_t S, int64_
         L = 0;
     if (L > S)
         L = S;
-    return (r < L) ? r + 1 : 0;
+    *c0 = 0;
+    *c1 = 0;
+    if (r >= L)
+        return;
+    if (kind == 1) {
+        *c1 = L;
+    } else {
+        *c1 = r + 1;
+        if (kind == 2 && r - window + 1 > 0)
+            *c0 = r - window + 1;
+    }
 }
 
 static int bad_shape(int64_t B, int64_t M, int64_t S, int64_t row_begin, int64_t row_end)
@@ -191,70 +214,91 @@ static int bad_shape(int64_t B, int64_t M, int64_t S, int64_t row_begin, int64_t
     return row_end > B * M * S;
 }
 
+static int bad_mask(int kind, int64_t window)
+{
+    return kind < 0 || kind > 2 || (kind == 2 && window < 1);
+}
+
 /* ---- forward ----
  * x: rows [row_begin, row_end) of X[B,M,S,S], contiguous, element type dtype.
  * y: (row_end - row_begin) * S doubles. */
-int gtms_oracle_forward(const void* x, int dtype, const int32_t* seq_lens,
-                        int64_t B, int64_t M, int64_t S, double scale,
-                        int64_t row_begin, int64_t row_end, double* y)
+int gtms_oracle_forward_masked(const void* x, int dtype, const int32_t* seq_lens,
+                               int64_t B, int64_t M, int64_t S, double scale, int kind, int64_t window,
+                               int64_t row_begin, int64_t row_end, double* y)
 {
-    if (dtype < ORC_F32 || dtype > ORC_F64 || bad_shape(B, M, S, row_begin, row_end))
+    if (dtype < ORC_F32 || dtype > ORC_F64 || bad_shape(B, M, S, row_begin, row_end) || bad_mask(kind, window))
         return ORC_BAD_ARG;
     for (int64_t q = row_begin; q < row_end; ++q) {
         const int64_t base = (q - row_begin) * S;
-        const int64_t n = kept_prefix(seq_lens, M, S, q);
+        int64_t c0, c1;
+        kept_range(seq_lens, M, S, kind, window, q, &c0, &c1);
         double* yr = y + base;
         for (int64_t c = 0; c < S; ++c)
             yr[c] = 0.0;
-        if (n == 0)
+        if (c1 <= c0)
             continue;
         /* z_c = scale * x_c; the row maximum is subtracted before exp so that
          * large scores cannot overflow (the result is unchanged mathematically). */
         double zmax = -INFINITY;
-        for (int64_t c = 0; c < n; ++c) {
+        for (int64_t c = c0; c < c1; ++c) {
             const double z = scale * load_elem(x, base + c, dtype);
             if (z > zmax)
                 zmax = z;
         }
         double sum = 0.0;
-        for (int64_t c = 0; c < n; ++c) {
+        for (int64_t c = c0; c < c1; ++c) {
             const double e = exp(scale * load_elem(x, base + c, dtype) - zmax);
             yr[c] = e;
             sum += e;
         }
-        for (int64_t c = 0; c < n; ++c)
+        for (int64_t c = c0; c < c1; ++c)
             yr[c] = yr[c] / sum;
     }
     return ORC_OK;
 }
 
+int gtms_oracle_forward(const void* x, int dtype, const int32_t* seq_lens,
+                        int64_t B, int64_t M, int64_t S, double scale,
+                        int64_t row_begin, int64_t row_end, double* y)
+{
+    return gtms_oracle_forward_masked(x, dtype, seq_lens, B, M, S, scale, 0, 0, row_begin, row_end, y);
+}
+
 /* ---- backward ----
  * y, dy: rows [row_begin, row_end), element type dtype (ORC_F64 accepted for
  * unrounded inputs). dx: (row_end - row_begin) * S doubles. */
-int gtms_oracle_backward(const void* y, const void* dy, int dtype, const int32_t* seq_lens,
-                         int64_t B, int64_t M, int64_t S, double scale,
-                         int64_t row_begin, int64_t row_end, double* dx)
+int gtms_oracle_backward_masked(const void* y, const void* dy, int dtype, const int32_t* seq_lens,
+                                int64_t B, int64_t M, int64_t S, double scale, int kind, int64_t window,
+                                int64_t row_begin, int64_t row_end, double* dx)
 {
-    if (dtype < ORC_F32 || dtype > ORC_F64 || bad_shape(B, M, S, row_begin, row_end))
+    if (dtype < ORC_F32 || dtype > ORC_F64 || bad_shape(B, M, S, row_begin, row_end) || bad_mask(kind, window))
         return ORC_BAD_ARG;
     for (int64_t q = row_begin; q < row_end; ++q) {
         const int64_t base = (q - row_begin) * S;
-        const int64_t n = kept_prefix(seq_lens, M, S, q);
+        int64_t c0, c1;
+        kept_range(seq_lens, M, S, kind, window, q, &c0, &c1);
         double* dxr = dx + base;
         for (int64_t c = 0; c < S; ++c)
             dxr[c] = 0.0;
-        if (n == 0)
+        if (c1 <= c0)
             continue;
-        double dot = 0.0;   /* sum_j dy_j * y_j over the kept prefix */
-        for (int64_t c = 0; c < n; ++c)
+        double dot = 0.0;   /* sum_j dy_j * y_j over the kept range */
+        for (int64_t c = c0; c < c1; ++c)
             dot += load_elem(dy, base + c, dtype) * load_elem(y, base + c, dtype);
-        for (int64_t c = 0; c < n; ++c) {
+        for (int64_t c = c0; c < c1; ++c) {
             const double yc = load_elem(y, base + c, dtype);
             const double dyc = load_elem(dy, base + c, dtype);
             dxr[c] = scale * yc * (dyc - dot);
         }
     }
     return ORC_OK;
+}
+
+int gtms_oracle_backward(const void* y, const void* dy, int dtype, const int32_t* seq_lens,
+                         int64_t B, int64_t M, int64_t S, double scale,
+                         int64_t row_begin, int64_t row_end, double* dx)
+{
+    return gtms_oracle_backward_masked(y, dy, dtype, seq_lens, B, M, S, scale, 0, 0, row_begin, row_end, dx);
 }
 
 /* ---- element conversion helpers (used by the tests to form expected bits) ---- */

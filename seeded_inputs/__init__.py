@@ -23,6 +23,10 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
 * ``s4096_bf16`` -- X[32,16,4096,4096] bf16 ~N(0, variance 4),
   seq_len ~ U{2048..4096}, scale 0.125, forward + backward: an added S=4096
   measurement point mirroring the ScaledMaskSoftmax article's 4096 row.
+* ``s16384_bf16`` -- X[4,8,16384,16384] bf16 ~N(0, variance 4),
+  seq_len ~ U{8192..16384}, scale 0.125, and ``s32768_bf16`` --
+  X[1,4,32768,32768], seq_len ~ U{16384..32768}: added measurement points for
+  rows split over a cluster of CTAs.
 * ``s1000_b2`` -- X[2,64,1000,1000], otherwise like ``s1000_b12``: a small
   stand-in for profiler captures.
 
@@ -103,6 +107,11 @@ WORKLOADS = {
                           spike_prob=0.01, spike_value=30.0, seed=20261207),
     "s4096_bf16": Workload("s4096_bf16", 32, 16, 4096, "bf16", 0.125, x_std=2.0,
                            seq_len_range=(2048, 4096), seed=20261208),
+    # rows longer than one CTA holds (a cluster of CTAs per row): added measurement points
+    "s16384_bf16": Workload("s16384_bf16", 4, 8, 16384, "bf16", 0.125, x_std=2.0,
+                            seq_len_range=(8192, 16384), seed=20261210),
+    "s32768_bf16": Workload("s32768_bf16", 1, 4, 32768, "bf16", 0.125, x_std=2.0,
+                            seq_len_range=(16384, 32768), seed=20261211),
     # profiling stand-in for s1000_b12: same distribution, 2 of the 12 batches
     # (2 GB on the device), small enough for a multi-pass ncu capture
     "s1000_b2": Workload("s1000_b2", 2, 64, 1000, "f32", 1.0, seq_len_range=(500, 1000), seed=20261209),

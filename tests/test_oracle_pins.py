@@ -381,3 +381,101 @@ def test_half_precision_inputs_are_decoded_exactly():
         a = oracle.forward(bits, sl, B, M, S, 0.125, code)
         b = oracle.forward(oracle.decode(bits, code), sl, B, M, S, 0.125, F64)
         assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# Mask families ("优化ScaledMaskSoftmax算子" section 6): length mask, sliding window
+# ---------------------------------------------------------------------------
+
+def _fwd64_kind(x, seq_lens, scale, kind, window=0):
+    B, M, S, _ = x.shape
+    y = oracle.forward(np.ascontiguousarray(x, np.float64), seq_lens, B, M, S, scale, F64, mask_kind=kind,
+                       window=window)
+    return y.reshape(B, M, S, S)
+
+
+def _bwd64_kind(y, dy, seq_lens, scale, kind, window=0):
+    B, M, S, _ = y.shape
+    dx = oracle.backward(np.ascontiguousarray(y, np.float64), np.ascontiguousarray(dy, np.float64), seq_lens,
+                         B, M, S, scale, F64, mask_kind=kind, window=window)
+    return dx.reshape(B, M, S, S)
+
+
+@pytest.mark.parametrize("S,L", [(6, 6), (20, 13), (33, 1), (16, 0)])
+def test_length_mask_matches_torch_key_padding_softmax(S, L):
+    """Kind 1: torch.softmax with a key-padding mask (c >= L masked), padded query rows zero."""
+    g = torch.Generator().manual_seed(200 + S + L)
+    x = torch.randn(2, 2, S, S, generator=g, dtype=torch.float64) * 2
+    scale = 0.9
+    key_pad = (torch.arange(S) >= L)[None, :].expand(S, S)
+    ref = torch.softmax((x * scale).masked_fill(key_pad, float("-inf")), dim=-1)
+    ref[:, :, L:, :] = 0.0
+    ref = torch.nan_to_num(ref, nan=0.0)
+    y = _fwd64_kind(x.numpy(), np.array([L, L], np.int32), scale, 1)
+    np.testing.assert_allclose(y, ref.numpy(), rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("S,L,w", [(9, 9, 3), (20, 15, 1), (20, 20, 7), (17, 10, 40)])
+def test_sliding_window_matches_torch_band_softmax(S, L, w):
+    """Kind 2: torch.softmax with a causal band of width w masked outside."""
+    g = torch.Generator().manual_seed(300 + S + L + w)
+    x = torch.randn(1, 3, S, S, generator=g, dtype=torch.float64) * 2
+    r = torch.arange(S)[:, None]
+    c = torch.arange(S)[None, :]
+    outside = (c > r) | (c <= r - w)
+    ref = torch.softmax((x * 0.6).masked_fill(outside, float("-inf")), dim=-1)
+    ref[:, :, L:, :] = 0.0
+    y = _fwd64_kind(x.numpy(), np.array([L], np.int32), 0.6, 2, w)
+    np.testing.assert_allclose(y, ref.numpy(), rtol=0, atol=1e-15)
+
+
+def test_window_special_cases():
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((2, 2, 12, 12)) * 3
+    sl = np.array([12, 7], np.int32)
+    # width 1: each live row keeps only its diagonal -> exactly one-hot
+    y1 = _fwd64_kind(x, sl, 1.3, 2, 1)
+    eye = np.eye(12)[None, None]
+    live = (np.arange(12)[None, :] < sl[:, None])[:, None, :, None]
+    assert np.array_equal(y1, np.broadcast_to(np.where(live, eye, 0.0), y1.shape))
+    # a window as wide as the row is the default grouped-tril op
+    assert np.array_equal(_fwd64_kind(x, sl, 1.3, 2, 12), _fwd64(x, sl, 1.3))
+    assert np.array_equal(_fwd64_kind(x, sl, 1.3, 2, 500), _fwd64(x, sl, 1.3))
+    # bad arguments: unknown kind, window < 1 for the sliding window
+    with pytest.raises(ValueError):
+        _fwd64_kind(x, sl, 1.0, 3)
+    with pytest.raises(ValueError):
+        _fwd64_kind(x, sl, 1.0, 2, 0)
+
+
+@pytest.mark.parametrize("kind,w", [(1, 0), (2, 3)])
+def test_mask_family_backward_matches_central_differences(kind, w):
+    S, scale, h = 6, 0.7, 1e-6
+    rng = np.random.default_rng(20 + kind)
+    x = rng.standard_normal((1, 1, S, S))
+    dy = rng.standard_normal((1, 1, S, S))
+    sl = np.array([5], np.int32)
+    y = _fwd64_kind(x, sl, scale, kind, w)
+    dx = _bwd64_kind(y, dy, sl, scale, kind, w)
+    num = np.zeros_like(x)
+    for r in range(S):
+        for c in range(S):
+            xp, xm = x.copy(), x.copy()
+            xp[0, 0, r, c] += h
+            xm[0, 0, r, c] -= h
+            num[0, 0, r, c] = ((_fwd64_kind(xp, sl, scale, kind, w) * dy).sum()
+                               - (_fwd64_kind(xm, sl, scale, kind, w) * dy).sum()) / (2 * h)
+    np.testing.assert_allclose(dx, num, rtol=0, atol=1e-8)
+
+
+@pytest.mark.parametrize("kind,w", [(0, 0), (1, 0), (2, 4)])
+def test_kept_ranges_match_oracle_zero_pattern(kind, w):
+    rng = np.random.default_rng(21)
+    S = 10
+    x = rng.standard_normal((3, 1, S, S))
+    sl = np.array([10, 6, 0], np.int32)
+    y = _fwd64_kind(x, sl, 1.0, kind, w)
+    c0, c1 = oracle.kept_ranges(sl, S, kind, w)
+    col = np.arange(S)[None, None, :]
+    kept = (col >= c0[:, :, None]) & (col < c1[:, :, None])
+    assert np.array_equal(y[:, 0] != 0.0, kept)
