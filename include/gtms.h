@@ -63,6 +63,22 @@ extern "C" {
 
 typedef enum { GTMS_F32 = 0, GTMS_BF16 = 1, GTMS_F16 = 2 } gtms_dtype;
 
+/*
+ * Mask families ("优化ScaledMaskSoftmax算子", section 6, lists a local window
+ * mask and a length mask next to the default). Each keeps a contiguous column
+ * range of a row r < L = clamp(seq_lens[b], 0, S) and nothing of rows r >= L:
+ *   GTMS_MASK_GROUPED_TRIL   c <= r                (the operator above)
+ *   GTMS_MASK_LENGTH         c < L                 (padded keys and queries)
+ *   GTMS_MASK_SLIDING_WINDOW r - window < c <= r   (causal band, window >= 1;
+ *                            the section's garbled local-window snippet is read
+ *                            as this band)
+ */
+typedef enum {
+    GTMS_MASK_GROUPED_TRIL = 0,
+    GTMS_MASK_LENGTH = 1,
+    GTMS_MASK_SLIDING_WINDOW = 2
+} gtms_mask_kind;
+
 typedef enum {
     GTMS_OK = 0,
     GTMS_ERR_INVALID_ARG = 1,
@@ -109,6 +125,19 @@ int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_le
  * enqueues nothing, allocates nothing.
  */
 int gtms_device_pointer_of_host(const void* host, void** device);
+
+/*
+ * gtms_forward / gtms_backward with another mask family (gtms_mask_kind).
+ * `window` is the band width of GTMS_MASK_SLIDING_WINDOW (>= 1; widths >= S
+ * give the grouped-tril op) and is ignored by the other kinds. An unknown kind
+ * is GTMS_ERR_UNSUPPORTED, a sliding window narrower than 1
+ * GTMS_ERR_INVALID_ARG; everything else is as for gtms_forward / gtms_backward
+ * (gtms_forward is gtms_forward_masked with GTMS_MASK_GROUPED_TRIL).
+ */
+int gtms_forward_masked(const void* x, void* y, const int32_t* seq_lens, int64_t B, int64_t M, int64_t S,
+                        float scale, int mask_kind, int64_t window, int dtype, void* stream);
+int gtms_backward_masked(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B, int64_t M,
+                         int64_t S, float scale, int mask_kind, int64_t window, int dtype, void* stream);
 
 /* Static, NUL-terminated name of a status code ("GTMS_OK", ...). */
 const char* gtms_status_string(int status);

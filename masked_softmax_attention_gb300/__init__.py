@@ -24,9 +24,11 @@ from ._build import LIB_PATH, build_library  # noqa: F401  (re-exported for buil
 GTMS_F32, GTMS_BF16, GTMS_F16 = 0, 1, 2
 GTMS_OK, GTMS_ERR_INVALID_ARG, GTMS_ERR_UNSUPPORTED, GTMS_ERR_CUDA = 0, 1, 2, 3
 GTMS_MAX_S = 65536
+GTMS_MASK_GROUPED_TRIL, GTMS_MASK_LENGTH, GTMS_MASK_SLIDING_WINDOW = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gtms_forward", "gtms_backward", "gtms_status_string", "gtms_version",
-                    "gtms_kernel_name", "gtms_device_pointer_of_host")
+                    "gtms_kernel_name", "gtms_device_pointer_of_host", "gtms_forward_masked",
+                    "gtms_backward_masked")
 
 _lib = None
 _lock = threading.Lock()
@@ -57,6 +59,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.gtms_forward.restype = ctypes.c_int
         lib.gtms_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
         lib.gtms_backward.restype = ctypes.c_int
+        lib.gtms_forward_masked.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, i64,
+                                            ctypes.c_int, vp]
+        lib.gtms_forward_masked.restype = ctypes.c_int
+        lib.gtms_backward_masked.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, i64,
+                                             ctypes.c_int, vp]
+        lib.gtms_backward_masked.restype = ctypes.c_int
         lib.gtms_status_string.argtypes = [ctypes.c_int]
         lib.gtms_status_string.restype = ctypes.c_char_p
         lib.gtms_version.argtypes = []
@@ -80,6 +88,14 @@ def gtms_forward(x, y, seq_lens, B, M, S, scale, dtype, stream) -> int:
 
 def gtms_backward(y, dy, dx, seq_lens, B, M, S, scale, dtype, stream) -> int:
     return load_library().gtms_backward(y, dy, dx, seq_lens, B, M, S, scale, dtype, stream)
+
+
+def gtms_forward_masked(x, y, seq_lens, B, M, S, scale, mask_kind, window, dtype, stream) -> int:
+    return load_library().gtms_forward_masked(x, y, seq_lens, B, M, S, scale, mask_kind, window, dtype, stream)
+
+
+def gtms_backward_masked(y, dy, dx, seq_lens, B, M, S, scale, mask_kind, window, dtype, stream) -> int:
+    return load_library().gtms_backward_masked(y, dy, dx, seq_lens, B, M, S, scale, mask_kind, window, dtype, stream)
 
 
 def status_string(status: int) -> str:
@@ -133,8 +149,8 @@ def _check_lens(seq_lens, B, device):
         raise ValueError("seq_lens must be a contiguous int32 CUDA tensor of shape [B] on the scores' device")
 
 
-def forward(x, seq_lens, scale: float = 1.0, out=None):
-    """y = grouped-tril masked softmax(scale * x); ``out`` may be ``x`` (in place)."""
+def forward(x, seq_lens, scale: float = 1.0, out=None, mask_kind: int = GTMS_MASK_GROUPED_TRIL, window: int = 0):
+    """y = masked softmax(scale * x) (grouped tril by default); ``out`` may be ``x`` (in place)."""
     import torch
 
     _check_scores("x", x)
@@ -144,14 +160,15 @@ def forward(x, seq_lens, scale: float = 1.0, out=None):
     if y.shape != x.shape or y.dtype != x.dtype or y.device != x.device or not y.is_contiguous():
         raise ValueError("out must match x in shape, dtype, device and be contiguous")
     stream = torch.cuda.current_stream(x.device).cuda_stream
-    rc = gtms_forward(x.data_ptr(), y.data_ptr(), seq_lens.data_ptr(), B, M, S, float(scale),
-                      _dtype_code(x), stream)
+    rc = gtms_forward_masked(x.data_ptr(), y.data_ptr(), seq_lens.data_ptr(), B, M, S, float(scale),
+                             int(mask_kind), int(window), _dtype_code(x), stream)
     if rc != GTMS_OK:
-        raise GtmsError("gtms_forward", rc)
+        raise GtmsError("gtms_forward_masked", rc)
     return y
 
 
-def backward(y, dy, seq_lens, scale: float = 1.0, out=None):
+def backward(y, dy, seq_lens, scale: float = 1.0, out=None, mask_kind: int = GTMS_MASK_GROUPED_TRIL,
+             window: int = 0):
     """dx = scale * y * (dy - rowsum(dy * y)) under the mask; ``out`` may be ``y`` or ``dy``."""
     import torch
 
@@ -165,10 +182,10 @@ def backward(y, dy, seq_lens, scale: float = 1.0, out=None):
     if dx.shape != y.shape or dx.dtype != y.dtype or dx.device != y.device or not dx.is_contiguous():
         raise ValueError("out must match y in shape, dtype, device and be contiguous")
     stream = torch.cuda.current_stream(y.device).cuda_stream
-    rc = gtms_backward(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), seq_lens.data_ptr(), B, M, S,
-                       float(scale), _dtype_code(y), stream)
+    rc = gtms_backward_masked(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), seq_lens.data_ptr(), B, M, S,
+                              float(scale), int(mask_kind), int(window), _dtype_code(y), stream)
     if rc != GTMS_OK:
-        raise GtmsError("gtms_backward", rc)
+        raise GtmsError("gtms_backward_masked", rc)
     return dx
 
 

@@ -15,20 +15,25 @@
 #define GTMS_EXPORT extern "C" __attribute__((visibility("default")))
 
 namespace gtms {
-template <typename T>
+template <typename T, int MK>
 void launch_forward(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
-template <typename T>
+template <typename T, int MK>
 void launch_backward(int, const void*, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
-extern template void launch_forward<float>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
-extern template void launch_forward<__nv_bfloat16>(int, const void*, void*, const int32_t*, const Geom&, float,
-                                                   cudaStream_t);
-extern template void launch_forward<__half>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
-extern template void launch_backward<float>(int, const void*, const void*, void*, const int32_t*, const Geom&, float,
-                                            cudaStream_t);
-extern template void launch_backward<__nv_bfloat16>(int, const void*, const void*, void*, const int32_t*,
-                                                    const Geom&, float, cudaStream_t);
-extern template void launch_backward<__half>(int, const void*, const void*, void*, const int32_t*, const Geom&,
-                                             float, cudaStream_t);
+// Instantiated one per translation unit (gtms_{fwd,bwd}_<dtype>_<mask>.cu).
+#define GTMS_EXTERN_FOR(T, MK) \
+    extern template void launch_forward<T, MK>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t); \
+    extern template void launch_backward<T, MK>(int, const void*, const void*, void*, const int32_t*, const Geom&, float, \
+                                                cudaStream_t);
+GTMS_EXTERN_FOR(float, 0)
+GTMS_EXTERN_FOR(float, 1)
+GTMS_EXTERN_FOR(float, 2)
+GTMS_EXTERN_FOR(__nv_bfloat16, 0)
+GTMS_EXTERN_FOR(__nv_bfloat16, 1)
+GTMS_EXTERN_FOR(__nv_bfloat16, 2)
+GTMS_EXTERN_FOR(__half, 0)
+GTMS_EXTERN_FOR(__half, 1)
+GTMS_EXTERN_FOR(__half, 2)
+#undef GTMS_EXTERN_FOR
 }  // namespace gtms
 
 namespace {
@@ -88,7 +93,7 @@ bool bad_alias(const void* out, const void* in, uint64_t bytes)
     return out != in && overlaps(out, bytes, in, bytes);
 }
 
-gtms::Geom make_geom(int direction, int64_t rows, int64_t M, int64_t S, int variant, int e)
+gtms::Geom make_geom(int direction, int64_t rows, int64_t M, int64_t S, int variant, int e, int64_t window)
 {
     const gtms::Variant v = gtms::variant_at(direction, e, variant);
     gtms::Geom g;
@@ -97,7 +102,40 @@ gtms::Geom make_geom(int direction, int64_t rows, int64_t M, int64_t S, int vari
     g.S = static_cast<int32_t>(S);
     g.units = static_cast<int32_t>(v.vec16 ? S * e / 16 : S);
     g.small = rows <= static_cast<int64_t>(UINT32_MAX) ? 1 : 0;
+    g.window = static_cast<int32_t>(window < S ? window : S);
     return g;
+}
+
+// Mask kind and window: kinds 0..2; the sliding window needs a width >= 1.
+int check_mask(int mask_kind, int64_t window)
+{
+    if (mask_kind < 0 || mask_kind > 2)
+        return GTMS_ERR_UNSUPPORTED;
+    if (mask_kind == 2 && window < 1)
+        return GTMS_ERR_INVALID_ARG;
+    return GTMS_OK;
+}
+
+template <typename T>
+void run_forward(int kind, int variant, const void* x, void* y, const int32_t* seq_lens, const gtms::Geom& g,
+                 float scale, cudaStream_t st)
+{
+    switch (kind) {
+    case 0: gtms::launch_forward<T, 0>(variant, x, y, seq_lens, g, scale, st); break;
+    case 1: gtms::launch_forward<T, 1>(variant, x, y, seq_lens, g, scale, st); break;
+    default: gtms::launch_forward<T, 2>(variant, x, y, seq_lens, g, scale, st); break;
+    }
+}
+
+template <typename T>
+void run_backward(int kind, int variant, const void* y, const void* dy, void* dx, const int32_t* seq_lens,
+                  const gtms::Geom& g, float scale, cudaStream_t st)
+{
+    switch (kind) {
+    case 0: gtms::launch_backward<T, 0>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    case 1: gtms::launch_backward<T, 1>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    default: gtms::launch_backward<T, 2>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    }
 }
 
 int launch_status()
@@ -107,12 +145,15 @@ int launch_status()
 
 }  // namespace
 
-GTMS_EXPORT int gtms_forward(const void* x, void* y, const int32_t* seq_lens, int64_t B, int64_t M, int64_t S,
-                             float scale, int dtype, void* stream)
+GTMS_EXPORT int gtms_forward_masked(const void* x, void* y, const int32_t* seq_lens, int64_t B, int64_t M,
+                                    int64_t S, float scale, int mask_kind, int64_t window, int dtype, void* stream)
 {
     const Checked c = check_shape(B, M, S, scale, dtype);
-    if (c.status != GTMS_OK || c.rows == 0)
+    if (c.status != GTMS_OK)
         return c.status;
+    const int mc = check_mask(mask_kind, window);
+    if (mc != GTMS_OK || c.rows == 0)
+        return mc;
     const int e = elem_bytes(dtype);
     if (!x || !y || !seq_lens)
         return GTMS_ERR_INVALID_ARG;
@@ -126,22 +167,32 @@ GTMS_EXPORT int gtms_forward(const void* x, void* y, const int32_t* seq_lens, in
     const int variant = gtms::pick_variant(0, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
-    const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e);
+    const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e, window);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
-    case GTMS_F32: gtms::launch_forward<float>(variant, x, y, seq_lens, g, scale, st); break;
-    case GTMS_BF16: gtms::launch_forward<__nv_bfloat16>(variant, x, y, seq_lens, g, scale, st); break;
-    default: gtms::launch_forward<__half>(variant, x, y, seq_lens, g, scale, st); break;
+    case GTMS_F32: run_forward<float>(mask_kind, variant, x, y, seq_lens, g, scale, st); break;
+    case GTMS_BF16: run_forward<__nv_bfloat16>(mask_kind, variant, x, y, seq_lens, g, scale, st); break;
+    default: run_forward<__half>(mask_kind, variant, x, y, seq_lens, g, scale, st); break;
     }
     return launch_status();
 }
 
-GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B, int64_t M,
-                              int64_t S, float scale, int dtype, void* stream)
+GTMS_EXPORT int gtms_forward(const void* x, void* y, const int32_t* seq_lens, int64_t B, int64_t M, int64_t S,
+                             float scale, int dtype, void* stream)
+{
+    return gtms_forward_masked(x, y, seq_lens, B, M, S, scale, GTMS_MASK_GROUPED_TRIL, 0, dtype, stream);
+}
+
+GTMS_EXPORT int gtms_backward_masked(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B,
+                                     int64_t M, int64_t S, float scale, int mask_kind, int64_t window, int dtype,
+                                     void* stream)
 {
     const Checked c = check_shape(B, M, S, scale, dtype);
-    if (c.status != GTMS_OK || c.rows == 0)
+    if (c.status != GTMS_OK)
         return c.status;
+    const int mc = check_mask(mask_kind, window);
+    if (mc != GTMS_OK || c.rows == 0)
+        return mc;
     const int e = elem_bytes(dtype);
     if (!y || !dy || !dx || !seq_lens)
         return GTMS_ERR_INVALID_ARG;
@@ -155,14 +206,20 @@ GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int
     const int variant = gtms::pick_variant(1, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
-    const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e);
+    const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e, window);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
-    case GTMS_F32: gtms::launch_backward<float>(variant, y, dy, dx, seq_lens, g, scale, st); break;
-    case GTMS_BF16: gtms::launch_backward<__nv_bfloat16>(variant, y, dy, dx, seq_lens, g, scale, st); break;
-    default: gtms::launch_backward<__half>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    case GTMS_F32: run_backward<float>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st); break;
+    case GTMS_BF16: run_backward<__nv_bfloat16>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st); break;
+    default: run_backward<__half>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st); break;
     }
     return launch_status();
+}
+
+GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B, int64_t M,
+                              int64_t S, float scale, int dtype, void* stream)
+{
+    return gtms_backward_masked(y, dy, dx, seq_lens, B, M, S, scale, GTMS_MASK_GROUPED_TRIL, 0, dtype, stream);
 }
 
 GTMS_EXPORT int gtms_device_pointer_of_host(const void* host, void** device)

@@ -1,0 +1,7 @@
+// Backward kernel instantiations: bf16 IO, mask kind 0 (tril).
+#include "gtms_launch.cuh"
+
+namespace gtms {
+template void launch_backward<__nv_bfloat16, 0>(int, const void*, const void*, void*, const int32_t*, const Geom&, float,
+                                         cudaStream_t);
+}  // namespace gtms

@@ -1,0 +1,6 @@
+// Forward kernel instantiations: f16 IO, mask kind 1 (length).
+#include "gtms_launch.cuh"
+
+namespace gtms {
+template void launch_forward<__half, 1>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+}  // namespace gtms

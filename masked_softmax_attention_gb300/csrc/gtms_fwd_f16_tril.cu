@@ -1,0 +1,6 @@
+// Forward kernel instantiations: f16 IO, mask kind 0 (tril).
+#include "gtms_launch.cuh"
+
+namespace gtms {
+template void launch_forward<__half, 0>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+}  // namespace gtms

@@ -1,20 +1,23 @@
 // gtms_kernels.cuh -- sm_103a kernels of the grouped-tril masked softmax.
 //
 // One "team" of threads owns one row of X[B,M,S,S] at a time: a warp for short
-// rows, a whole CTA for long ones. The kept set of row r in batch b is the
-// prefix [0, n) with n = r + 1 if r < L_b else 0, L_b = clamp(seq_lens[b], 0, S)
-// ("Attention-Mask-Optimization" README, operator behaviour: kept iff r < L,
-// c < L and c <= r; c <= r < L already implies c < L). The mask is this one
-// comparison per row; no mask tensor exists ("实现思路": compute instead of
-// loading).
+// rows, a whole CTA for long ones (rows longer than one CTA holds go to the
+// cluster kernels of gtms_cluster.cuh). The kept set of row r in batch b is a
+// contiguous column range [c0, c1) computed from (r, L_b, mask kind), with
+// L_b = clamp(seq_lens[b], 0, S). For the default op ("Attention-Mask-
+// Optimization" README, operator behaviour: kept iff r < L, c < L and c <= r)
+// it is the prefix [0, r + 1) of rows r < L, since c <= r < L already implies
+// c < L. The mask is this computation per row; no mask tensor exists
+// ("实现思路": compute instead of loading).
 //
 // Per row, a team
-//   1. issues loads of only the access units that cover [0, n) (padded rows: none),
-//   2. issues the zero stores of every unit past the kept prefix right away --
-//      they depend on no load, so they overlap the load latency,
+//   1. issues loads of only the access units that cover [c0, c1) (padded rows: none),
+//   2. issues the zero stores of every unit outside them right away -- they
+//      depend on no load, so they overlap the load latency,
 //   3. reduces in fp32 with warp shuffles and, for CTA teams, one shared-memory
 //      exchange per reduction,
-//   4. writes the kept units (the masked elements of the last, partial unit as +0.0).
+//   4. writes the kept units (the masked elements of the first and last,
+//      partial units as +0.0).
 // Every unit is loaded and stored by the same thread, so an output may alias its
 // input exactly.
 //
@@ -23,7 +26,7 @@
 //     elements are handled as fp32 pairs with the packed f32x2 instructions of
 //     sm_100+ (__fadd2_rn / __fmul2_rn / __ffma2_rn); the exponential is one
 //     ex2.approx.f32 per kept element, kept in registers between the sum and
-//     the store; masking touches only the row's last, partial unit;
+//     the store; masking touches only the partial units at the range's ends;
 //   * element kernels (one element per unit) for rows that are not 16-byte
 //     multiples or buffers that are only element-aligned.
 //
@@ -54,6 +57,7 @@ struct Geom {
     int32_t S;
     int32_t units;        // access units per row (16-byte vectors, or elements)
     int32_t small;        // rows fits in 32 bits: use 32-bit division
+    int32_t window;       // width of the sliding causal window (mask kind 2)
 
     __device__ __forceinline__ void locate(int64_t q, int32_t& b, int32_t& r) const
     {
@@ -68,12 +72,33 @@ struct Geom {
     }
 };
 
-__device__ __forceinline__ int32_t kept_prefix(const int32_t* __restrict__ seq_lens, int32_t b, int32_t r,
-                                               int32_t S)
+// Mask families: every kind keeps a contiguous column range [c0, c1) of a row
+// r < L and nothing of the rows r >= L ("优化ScaledMaskSoftmax算子", section 6,
+// lists the length mask and the local window besides the default):
+//   kMaskGroupedTril (0): [0, r + 1)                 -- the README's operator
+//   kMaskLength      (1): [0, L)                     -- padded keys and queries
+//   kMaskWindow      (2): [max(0, r - w + 1), r + 1) -- causal band of width w
+constexpr int kMaskGroupedTril = 0;
+constexpr int kMaskLength = 1;
+constexpr int kMaskWindow = 2;
+
+template <int MK>
+__device__ __forceinline__ void kept_range(const int32_t* __restrict__ seq_lens, int32_t b, int32_t r,
+                                           const Geom& g, int32_t& c0, int32_t& c1)
 {
     int32_t L = __ldg(seq_lens + b);
-    L = L < 0 ? 0 : (L > S ? S : L);
-    return r < L ? r + 1 : 0;
+    L = L < 0 ? 0 : (L > g.S ? g.S : L);
+    c0 = 0;
+    c1 = 0;
+    if (r < L) {
+        if constexpr (MK == kMaskLength) {
+            c1 = L;
+        } else {
+            c1 = r + 1;
+            if constexpr (MK == kMaskWindow)
+                c0 = r - g.window + 1 > 0 ? r - g.window + 1 : 0;
+        }
+    }
 }
 
 template <int TW>
@@ -233,12 +258,12 @@ template <> struct Pairs<float> {
         u.w[2 * p] = __float_as_uint(v.x);
         u.w[2 * p + 1] = __float_as_uint(v.y);
     }
-    // Zero the raw bits of elements e >= vc.
-    __device__ static void clear_from(Unit16& u, int vc)
+    // Zero the raw bits of elements outside [lo, hi).
+    __device__ static void clear_outside(Unit16& u, int lo, int hi)
     {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            if (e >= vc)
+            if (e < lo || e >= hi)
                 u.w[e] = 0u;
     }
 };
@@ -255,11 +280,11 @@ template <> struct Pairs<__nv_bfloat16> {
         const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
         u.w[p] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    __device__ static void clear_from(Unit16& u, int vc)
+    __device__ static void clear_outside(Unit16& u, int lo, int hi)
     {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            if (e >= vc)
+            if (e < lo || e >= hi)
                 u.w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
     }
 };
@@ -276,32 +301,243 @@ template <> struct Pairs<__half> {
         const __half2 h = __floats2half2_rn(v.x, v.y);
         u.w[p] = *reinterpret_cast<const uint32_t*>(&h);
     }
-    __device__ static void clear_from(Unit16& u, int vc)
+    __device__ static void clear_outside(Unit16& u, int lo, int hi)
     {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            if (e >= vc)
+            if (e < lo || e >= hi)
                 u.w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
     }
 };
 
 // ---------------------------------------------------------------------------
-// Vector forward: y = masked softmax(scale * x).
+// Unit range of a kept column range: units [u0, u1) hold kept elements; only
+// the first and the last of them can be partial (element e of unit j is kept
+// iff lo <= e < hi with lo = c0 - j*EPU, hi = c1 - j*EPU).
+// ---------------------------------------------------------------------------
+struct UnitRange {
+    int32_t c0, c1, u0, u1;
+
+    template <int EPU>
+    __device__ __forceinline__ static UnitRange of(int32_t c0, int32_t c1)
+    {
+        UnitRange u{c0, c1, c0 / EPU, (c1 + EPU - 1) / EPU};
+        if (c1 <= c0)
+            u.u0 = u.u1 = 0;
+        return u;
+    }
+    __device__ __forceinline__ bool kept(int j) const { return j >= u0 && j < u1; }
+};
+
+// ---------------------------------------------------------------------------
+// Row stages shared by the per-row vector kernels and the cluster kernels. A
+// thread holds NV slots; unit_of(k) is the row unit of slot k (row units are
+// 16 bytes; UnitOf differs only in how slots interleave across the team).
+// ---------------------------------------------------------------------------
+
+// Loads of the kept units only.
+template <int NV, typename UnitOf>
+__device__ __forceinline__ void load_kept(const char* row, const UnitRange& ur, UnitOf unit_of, Unit16 (&raw)[NV])
+{
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (ur.kept(j))
+            raw[k] = load16(row + 16 * j);
+    }
+}
+
+// +0.0 stores of every unit of the row that holds no kept element.
+template <int NV, typename UnitOf>
+__device__ __forceinline__ void store_zeros(char* row, const UnitRange& ur, int units, UnitOf unit_of)
+{
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (j < units && !ur.kept(j))
+            store16(row + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
+    }
+}
+
+// Decode the kept units into fp32 pairs and return this thread's extreme (max
+// when use_max, else min). Masked elements of a partial unit become the
+// neutral value (-inf / +inf), so they can never be the extreme.
+template <typename T, int NV, typename UnitOf>
+__device__ __forceinline__ float fwd_decode_extreme(const Unit16 (&raw)[NV], float2 (&v)[NV][Pairs<T>::kPairs],
+                                                    const UnitRange& ur, UnitOf unit_of, bool use_max)
+{
+    using IO = Pairs<T>;
+    constexpr int PPU = IO::kPairs, EPU = 2 * PPU;
+    const float neutral = use_max ? -INFINITY : INFINITY;
+    float ext = neutral;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (ur.kept(j)) {
+#pragma unroll
+            for (int p = 0; p < PPU; ++p)
+                v[k][p] = IO::get(raw[k], p);
+            const int lo = ur.c0 - j * EPU, hi = ur.c1 - j * EPU;
+            if (lo > 0 || hi < EPU) {
+#pragma unroll
+                for (int p = 0; p < PPU; ++p) {
+                    if (2 * p < lo || 2 * p >= hi)
+                        v[k][p].x = neutral;
+                    if (2 * p + 1 < lo || 2 * p + 1 >= hi)
+                        v[k][p].y = neutral;
+                }
+            }
+            if (use_max) {
+#pragma unroll
+                for (int p = 0; p < PPU; ++p)
+                    ext = max3(ext, v[k][p].x, v[k][p].y);
+            } else {
+#pragma unroll
+                for (int p = 0; p < PPU; ++p)
+                    ext = min3(ext, v[k][p].x, v[k][p].y);
+            }
+        }
+    }
+    return ext;
+}
+
+// Replace the pairs by 2^((x - ext) * c) (masked elements 0) and return this
+// thread's sum of them.
+template <typename T, int NV, typename UnitOf>
+__device__ __forceinline__ float fwd_exp_sum(float2 (&v)[NV][Pairs<T>::kPairs], const UnitRange& ur, UnitOf unit_of,
+                                             float ext, float c)
+{
+    constexpr int PPU = Pairs<T>::kPairs, EPU = 2 * PPU;
+    const float2 shift = splat2(-ext), c2 = splat2(c);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (ur.kept(j)) {
+#pragma unroll
+            for (int p = 0; p < PPU; ++p) {
+                const float2 t = __fmul2_rn(__fadd2_rn(v[k][p], shift), c2);
+                v[k][p] = make_float2(ex2(t.x), ex2(t.y));
+            }
+            const int lo = ur.c0 - j * EPU, hi = ur.c1 - j * EPU;
+            if (lo > 0 || hi < EPU) {
+#pragma unroll
+                for (int p = 0; p < PPU; ++p) {
+                    if (2 * p < lo || 2 * p >= hi)
+                        v[k][p].x = 0.0f;
+                    if (2 * p + 1 < lo || 2 * p + 1 >= hi)
+                        v[k][p].y = 0.0f;
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < PPU; ++p)
+                acc = __fadd2_rn(acc, v[k][p]);
+        }
+    }
+    return __fadd_rn(acc.x, acc.y);
+}
+
+// Store y = e * f for the kept units (masked elements of partial units are
+// already 0, so they store as +0.0).
+template <typename T, int NV, typename UnitOf>
+__device__ __forceinline__ void fwd_store(char* row, const float2 (&v)[NV][Pairs<T>::kPairs], const UnitRange& ur,
+                                          UnitOf unit_of, float f)
+{
+    using IO = Pairs<T>;
+    const float2 f2 = splat2(f);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (ur.kept(j)) {
+            Unit16 o;
+#pragma unroll
+            for (int p = 0; p < IO::kPairs; ++p)
+                IO::put(o, p, __fmul2_rn(v[k][p], f2));
+            store16(row + 16 * j, o);
+        }
+    }
+}
+
+// Backward: zero the masked elements of partial units (also clears any NaN
+// there), then return this thread's float-float dot sum(dy * y) in (hi, lo).
+template <typename T, int NV, typename UnitOf>
+__device__ __forceinline__ void bwd_dot(Unit16 (&ry)[NV], Unit16 (&rg)[NV], const UnitRange& ur, UnitOf unit_of,
+                                        float& hi, float& lo)
+{
+    using IO = Pairs<T>;
+    constexpr int PPU = IO::kPairs, EPU = 2 * PPU;
+    float2 hi2 = make_float2(0.0f, 0.0f), lo2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (ur.kept(j)) {
+            const int lo_e = ur.c0 - j * EPU, hi_e = ur.c1 - j * EPU;
+            if (lo_e > 0 || hi_e < EPU) {
+                IO::clear_outside(ry[k], lo_e, hi_e);
+                IO::clear_outside(rg[k], lo_e, hi_e);
+            }
+#pragma unroll
+            for (int p = 0; p < PPU; ++p) {
+                const float2 a = IO::get(ry[k], p), cdy = IO::get(rg[k], p);
+                const float2 pr = __fmul2_rn(a, cdy);
+                const float2 s = __fadd2_rn(hi2, pr);
+                const float2 bb = __fadd2_rn(s, neg2(hi2));
+                const float2 e = __fadd2_rn(__fadd2_rn(hi2, neg2(__fadd2_rn(s, neg2(bb)))), __fadd2_rn(pr, neg2(bb)));
+                if constexpr (IO::kExactProducts) {
+                    lo2 = __fadd2_rn(lo2, e);
+                } else {
+                    const float2 pe = __ffma2_rn(a, cdy, neg2(pr));
+                    lo2 = __fadd2_rn(lo2, __fadd2_rn(e, pe));
+                }
+                hi2 = s;
+            }
+        }
+    }
+    float e0;
+    two_sum(hi2.x, hi2.y, hi, e0);
+    lo = __fadd_rn(__fadd_rn(lo2.x, lo2.y), e0);
+}
+
+// Backward: store dx = scale * y * ((dy - dh) - dl) for the kept units, +0.0
+// bits at masked elements.
+template <typename T, int NV, typename UnitOf>
+__device__ __forceinline__ void bwd_store(char* row, const Unit16 (&ry)[NV], const Unit16 (&rg)[NV],
+                                          const UnitRange& ur, UnitOf unit_of, float dh, float dl, float scale)
+{
+    using IO = Pairs<T>;
+    constexpr int PPU = IO::kPairs, EPU = 2 * PPU;
+    const float2 ndh = splat2(-dh), ndl = splat2(-dl), sc = splat2(scale);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (ur.kept(j)) {
+            Unit16 o;
+#pragma unroll
+            for (int p = 0; p < PPU; ++p) {
+                const float2 a = IO::get(ry[k], p), cdy = IO::get(rg[k], p);
+                const float2 diff = __fadd2_rn(__fadd2_rn(cdy, ndh), ndl);
+                IO::put(o, p, __fmul2_rn(__fmul2_rn(a, diff), sc));
+            }
+            const int lo_e = ur.c0 - j * EPU, hi_e = ur.c1 - j * EPU;
+            if (lo_e > 0 || hi_e < EPU)
+                IO::clear_outside(o, lo_e, hi_e);
+            store16(row + 16 * j, o);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Vector forward: y = masked softmax(scale * x), one team per row.
 //
 // t = (x - x_ext) * (scale * log2 e) with x_ext the row max (scale >= 0) or min
 // (scale < 0): t <= 0 everywhere and exactly 0 at the extreme element, so a
 // one-element row gives exp = 1, sum = 1, y = 1.
-// Masked elements of the partial unit are first set to element 0 of that unit
-// (which is kept), so they cannot move the extreme, then their exponentials are
-// set to 0 before the sum.
 // ---------------------------------------------------------------------------
-template <typename T, int TW, int NV, int MINB>
+template <typename T, int MK, int TW, int NV, int MINB>
 __global__ void __launch_bounds__(TW == 32 ? kWarpTeamBlock : TW, MINB)
 gtms_fwd_vec_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
-    using IO = Pairs<T>;
-    constexpr int PPU = IO::kPairs;
-    constexpr int EPU = 2 * PPU;
+    constexpr int EPU = 2 * Pairs<T>::kPairs;
     __shared__ float red[TW > 32 ? 2 * (TW / 32) : 1];
 
     const float c = __fmul_rn(scale, kLog2e);
@@ -309,118 +545,39 @@ gtms_fwd_vec_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom
     int tid;
     int64_t team, nteams;
     team_coords<TW>(tid, team, nteams);
+    const auto unit_of = [tid](int k) { return tid + k * TW; };
 
     for (int64_t q = team; q < g.rows; q += nteams) {
-        int32_t b, r;
+        int32_t b, r, c0, c1;
         g.locate(q, b, r);
-        const int32_t n = kept_prefix(seq_lens, b, r, g.S);
-        const int32_t nu = (n + EPU - 1) / EPU;
+        kept_range<MK>(seq_lens, b, r, g, c0, c1);
+        const UnitRange ur = UnitRange::of<EPU>(c0, c1);
         const char* xr = reinterpret_cast<const char*>(x + q * g.S);
         char* yr = reinterpret_cast<char*>(y + q * g.S);
 
         Unit16 raw[NV];
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j < nu)
-                raw[k] = load16(xr + 16 * j);
-        }
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j >= nu && j < g.units)
-                store16(yr + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
-        }
-        if (n == 0)
+        load_kept<NV>(xr, ur, unit_of, raw);
+        store_zeros<NV>(yr, ur, g.units, unit_of);
+        if (c1 <= c0)
             continue;   // uniform across the team
 
-        float2 v[NV][PPU];
-        float ext = use_max ? -INFINITY : INFINITY;
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j < nu) {
-#pragma unroll
-                for (int p = 0; p < PPU; ++p)
-                    v[k][p] = IO::get(raw[k], p);
-                if (j == nu - 1) {
-                    const int vc = n - j * EPU;
-#pragma unroll
-                    for (int p = 0; p < PPU; ++p) {
-                        if (2 * p >= vc)
-                            v[k][p].x = v[k][0].x;
-                        if (2 * p + 1 >= vc)
-                            v[k][p].y = v[k][0].x;
-                    }
-                }
-                if (use_max) {
-#pragma unroll
-                    for (int p = 0; p < PPU; ++p)
-                        ext = max3(ext, v[k][p].x, v[k][p].y);
-                } else {
-#pragma unroll
-                    for (int p = 0; p < PPU; ++p)
-                        ext = min3(ext, v[k][p].x, v[k][p].y);
-                }
-            }
-        }
+        float2 v[NV][Pairs<T>::kPairs];
+        float ext = fwd_decode_extreme<T, NV>(raw, v, ur, unit_of, use_max);
         ext = use_max ? team_max<TW>(ext, red) : -team_max<TW>(-ext, red);
-
-        const float2 shift = splat2(-ext), c2 = splat2(c);
-        float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j < nu) {
-#pragma unroll
-                for (int p = 0; p < PPU; ++p) {
-                    const float2 t = __fmul2_rn(__fadd2_rn(v[k][p], shift), c2);
-                    v[k][p] = make_float2(ex2(t.x), ex2(t.y));
-                }
-                if (j == nu - 1) {
-                    const int vc = n - j * EPU;
-#pragma unroll
-                    for (int p = 0; p < PPU; ++p) {
-                        if (2 * p >= vc)
-                            v[k][p].x = 0.0f;
-                        if (2 * p + 1 >= vc)
-                            v[k][p].y = 0.0f;
-                    }
-                }
-#pragma unroll
-                for (int p = 0; p < PPU; ++p)
-                    acc = __fadd2_rn(acc, v[k][p]);
-            }
-        }
-        const float s = team_sum<TW>(__fadd_rn(acc.x, acc.y), red + (TW > 32 ? TW / 32 : 0));
-        const float2 inv = splat2(__frcp_rn(s));
-
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j < nu) {
-                Unit16 o;
-#pragma unroll
-                for (int p = 0; p < PPU; ++p)
-                    IO::put(o, p, __fmul2_rn(v[k][p], inv));
-                store16(yr + 16 * j, o);
-            }
-        }
+        const float s = team_sum<TW>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), red + (TW > 32 ? TW / 32 : 0));
+        fwd_store<T, NV>(yr, v, ur, unit_of, __frcp_rn(s));
     }
 }
 
 // ---------------------------------------------------------------------------
-// Vector backward: dx = scale * y * (dy - rowsum(dy * y)).
-// The raw units of y and dy stay in registers (masked elements of the partial
-// unit zeroed, which also neutralises any NaN there); each pass decodes them.
+// Vector backward: dx = scale * y * (dy - rowsum(dy * y)), one team per row.
+// The raw units of y and dy stay in registers; each pass decodes them.
 // ---------------------------------------------------------------------------
-template <typename T, int TW, int NV, int MINB>
+template <typename T, int MK, int TW, int NV, int MINB>
 __global__ void __launch_bounds__(TW == 32 ? kWarpTeamBlock : TW, MINB)
 gtms_bwd_vec_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
-    using IO = Pairs<T>;
-    constexpr int PPU = IO::kPairs;
-    constexpr int EPU = 2 * PPU;
+    constexpr int EPU = 2 * Pairs<T>::kPairs;
     // Two buffers, alternating per reduced row: with a single exchange per row a
     // fast warp could otherwise overwrite a slot that a slow warp is still reading.
     __shared__ float red[2][TW > 32 ? 2 * (TW / 32) : 1];
@@ -429,88 +586,31 @@ gtms_bwd_vec_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__ 
     int tid;
     int64_t team, nteams;
     team_coords<TW>(tid, team, nteams);
-    const float2 sc = splat2(scale);
+    const auto unit_of = [tid](int k) { return tid + k * TW; };
 
     for (int64_t q = team; q < g.rows; q += nteams) {
-        int32_t b, r;
+        int32_t b, r, c0, c1;
         g.locate(q, b, r);
-        const int32_t n = kept_prefix(seq_lens, b, r, g.S);
-        const int32_t nu = (n + EPU - 1) / EPU;
+        kept_range<MK>(seq_lens, b, r, g, c0, c1);
+        const UnitRange ur = UnitRange::of<EPU>(c0, c1);
         const char* yr = reinterpret_cast<const char*>(y + q * g.S);
         const char* gr = reinterpret_cast<const char*>(dy + q * g.S);
         char* dr = reinterpret_cast<char*>(dx + q * g.S);
 
         Unit16 ry[NV], rg[NV];
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j < nu) {
-                ry[k] = load16(yr + 16 * j);
-                rg[k] = load16(gr + 16 * j);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j >= nu && j < g.units)
-                store16(dr + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
-        }
-        if (n == 0)
+        load_kept<NV>(yr, ur, unit_of, ry);
+        load_kept<NV>(gr, ur, unit_of, rg);
+        store_zeros<NV>(dr, ur, g.units, unit_of);
+        if (c1 <= c0)
             continue;
 
-        float2 hi2 = make_float2(0.0f, 0.0f), lo2 = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j < nu) {
-                if (j == nu - 1) {
-                    const int vc = n - j * EPU;
-                    IO::clear_from(ry[k], vc);
-                    IO::clear_from(rg[k], vc);
-                }
-#pragma unroll
-                for (int p = 0; p < PPU; ++p) {
-                    const float2 a = IO::get(ry[k], p), cdy = IO::get(rg[k], p);
-                    const float2 pr = __fmul2_rn(a, cdy);
-                    const float2 s = __fadd2_rn(hi2, pr);
-                    const float2 bb = __fadd2_rn(s, neg2(hi2));
-                    const float2 e = __fadd2_rn(__fadd2_rn(hi2, neg2(__fadd2_rn(s, neg2(bb)))),
-                                                __fadd2_rn(pr, neg2(bb)));
-                    if constexpr (IO::kExactProducts) {
-                        lo2 = __fadd2_rn(lo2, e);
-                    } else {
-                        const float2 pe = __ffma2_rn(a, cdy, neg2(pr));
-                        lo2 = __fadd2_rn(lo2, __fadd2_rn(e, pe));
-                    }
-                    hi2 = s;
-                }
-            }
-        }
-        float hi, lo, e0;
-        two_sum(hi2.x, hi2.y, hi, e0);
-        lo = __fadd_rn(__fadd_rn(lo2.x, lo2.y), e0);
+        float hi, lo;
+        bwd_dot<T, NV>(ry, rg, ur, unit_of, hi, lo);
         team_ff_sum<TW>(hi, lo, red[par]);
         par ^= 1;
         const float dh = __fadd_rn(hi, lo);
         const float dl = __fsub_rn(lo, __fsub_rn(dh, hi));
-        const float2 ndh = splat2(-dh), ndl = splat2(-dl);
-
-#pragma unroll
-        for (int k = 0; k < NV; ++k) {
-            const int j = tid + k * TW;
-            if (j < nu) {
-                Unit16 o;
-#pragma unroll
-                for (int p = 0; p < PPU; ++p) {
-                    const float2 a = IO::get(ry[k], p), cdy = IO::get(rg[k], p);
-                    const float2 diff = __fadd2_rn(__fadd2_rn(cdy, ndh), ndl);
-                    IO::put(o, p, __fmul2_rn(__fmul2_rn(a, diff), sc));
-                }
-                if (j == nu - 1)
-                    IO::clear_from(o, n - j * EPU);   // masked outputs are +0.0 bits
-                store16(dr + 16 * j, o);
-            }
-        }
+        bwd_store<T, NV>(dr, ry, rg, ur, unit_of, dh, dl, scale);
     }
 }
 
@@ -537,7 +637,7 @@ template <> struct Elem<__half> {
     __device__ static Raw put(float v) { return __half_as_ushort(__float2half_rn(v)); }
 };
 
-template <typename T, int TW, int NV>
+template <typename T, int MK, int TW, int NV>
 __global__ void __launch_bounds__(TW == 32 ? kWarpTeamBlock : TW)
 gtms_fwd_elem_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
@@ -552,9 +652,9 @@ gtms_fwd_elem_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geo
     team_coords<TW>(tid, team, nteams);
 
     for (int64_t q = team; q < g.rows; q += nteams) {
-        int32_t b, r;
+        int32_t b, r, c0, c1;
         g.locate(q, b, r);
-        const int32_t n = kept_prefix(seq_lens, b, r, g.S);
+        kept_range<MK>(seq_lens, b, r, g, c0, c1);
         const Raw* xr = reinterpret_cast<const Raw*>(x + q * g.S);
         Raw* yr = reinterpret_cast<Raw*>(y + q * g.S);
 
@@ -562,44 +662,48 @@ gtms_fwd_elem_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geo
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
-            if (j < n)
+            if (j >= c0 && j < c1)
                 v[k] = E::get(xr[j]);
         }
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
-            if (j >= n && j < g.S)
+            if ((j < c0 || j >= c1) && j < g.S)
                 yr[j] = Raw(0);
         }
-        if (n == 0)
+        if (c1 <= c0)
             continue;
 
         float ext = use_max ? -INFINITY : INFINITY;
 #pragma unroll
-        for (int k = 0; k < NV; ++k)
-            if (tid + k * TW < n)
+        for (int k = 0; k < NV; ++k) {
+            const int j = tid + k * TW;
+            if (j >= c0 && j < c1)
                 ext = use_max ? fmaxf(ext, v[k]) : fminf(ext, v[k]);
+        }
         ext = use_max ? team_max<TW>(ext, red) : -team_max<TW>(-ext, red);
 
         float s = 0.0f;
 #pragma unroll
-        for (int k = 0; k < NV; ++k)
-            if (tid + k * TW < n) {
+        for (int k = 0; k < NV; ++k) {
+            const int j = tid + k * TW;
+            if (j >= c0 && j < c1) {
                 v[k] = ex2(__fmul_rn(__fsub_rn(v[k], ext), c));
                 s = __fadd_rn(s, v[k]);
             }
+        }
         s = team_sum<TW>(s, red + (TW > 32 ? TW / 32 : 0));
         const float inv = __frcp_rn(s);
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
-            if (j < n)
+            if (j >= c0 && j < c1)
                 yr[j] = E::put(__fmul_rn(v[k], inv));
         }
     }
 }
 
-template <typename T, int TW, int NV>
+template <typename T, int MK, int TW, int NV>
 __global__ void __launch_bounds__(TW == 32 ? kWarpTeamBlock : TW)
 gtms_bwd_elem_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
@@ -613,9 +717,9 @@ gtms_bwd_elem_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__
     team_coords<TW>(tid, team, nteams);
 
     for (int64_t q = team; q < g.rows; q += nteams) {
-        int32_t b, r;
+        int32_t b, r, c0, c1;
         g.locate(q, b, r);
-        const int32_t n = kept_prefix(seq_lens, b, r, g.S);
+        kept_range<MK>(seq_lens, b, r, g, c0, c1);
         const Raw* yr = reinterpret_cast<const Raw*>(y + q * g.S);
         const Raw* gr = reinterpret_cast<const Raw*>(dy + q * g.S);
         Raw* dr = reinterpret_cast<Raw*>(dx + q * g.S);
@@ -624,7 +728,7 @@ gtms_bwd_elem_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
-            if (j < n) {
+            if (j >= c0 && j < c1) {
                 vy[k] = E::get(yr[j]);
                 vg[k] = E::get(gr[j]);
             }
@@ -632,16 +736,17 @@ gtms_bwd_elem_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
-            if (j >= n && j < g.S)
+            if ((j < c0 || j >= c1) && j < g.S)
                 dr[j] = Raw(0);
         }
-        if (n == 0)
+        if (c1 <= c0)
             continue;
 
         float hi = 0.0f, lo = 0.0f;
 #pragma unroll
-        for (int k = 0; k < NV; ++k)
-            if (tid + k * TW < n) {
+        for (int k = 0; k < NV; ++k) {
+            const int j = tid + k * TW;
+            if (j >= c0 && j < c1) {
                 const float p = __fmul_rn(vy[k], vg[k]);
                 const float pe = __fmaf_rn(vy[k], vg[k], -p);
                 float s, e;
@@ -649,6 +754,7 @@ gtms_bwd_elem_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__
                 hi = s;
                 lo = __fadd_rn(lo, __fadd_rn(e, pe));
             }
+        }
         team_ff_sum<TW>(hi, lo, red[par]);
         par ^= 1;
         const float dh = __fadd_rn(hi, lo);
@@ -656,7 +762,7 @@ gtms_bwd_elem_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
-            if (j < n)
+            if (j >= c0 && j < c1)
                 dr[j] = E::put(__fmul_rn(__fmul_rn(vy[k], __fsub_rn(__fsub_rn(vg[k], dh), dl)), scale));
         }
     }

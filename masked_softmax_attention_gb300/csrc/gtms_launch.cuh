@@ -30,18 +30,18 @@ inline unsigned cluster_grid_for(int64_t rows)
     return static_cast<unsigned>((rows > cap ? cap : rows) * C);
 }
 
-template <typename T>
-void launch_forward(int id, const void* x, void* y, const int32_t* seq_lens, const Geom& g, float scale,
-                    cudaStream_t st)
+template <typename T, int MK>
+void launch_forward_mk(int id, const void* x, void* y, const int32_t* seq_lens, const Geom& g, float scale,
+                       cudaStream_t st)
 {
     const T* xp = static_cast<const T*>(x);
     T* yp = static_cast<T*>(y);
 #define GTMS_FWD_VEC_CASE(vid, tw, nv, mb) \
-    case vid: gtms_fwd_vec_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
+    case vid: gtms_fwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
 #define GTMS_FWD_ELEM_CASE(vid, tw, nv) \
-    case kElemBase + vid: gtms_fwd_elem_kernel<T, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
+    case kElemBase + vid: gtms_fwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
 #define GTMS_FWD_CL_CASE(vid, cl, tw, nv, mb) \
-    case kClusterBase + vid: gtms_fwd_cluster_kernel<T, cl, tw, nv, mb><<<cluster_grid_for<cl>(g.rows), tw, 0, st>>>(xp, yp, seq_lens, g, scale); break;
+    case kClusterBase + vid: gtms_fwd_cluster_kernel<T, MK, cl, tw, nv, mb><<<cluster_grid_for<cl>(g.rows), tw, 0, st>>>(xp, yp, seq_lens, g, scale); break;
     if constexpr (sizeof(T) == 4) {
         switch (id) { GTMS_FWD_VEC4(GTMS_FWD_VEC_CASE) GTMS_ELEM(GTMS_FWD_ELEM_CASE) GTMS_FWD_CL4(GTMS_FWD_CL_CASE) default: break; }
     } else {
@@ -52,19 +52,19 @@ void launch_forward(int id, const void* x, void* y, const int32_t* seq_lens, con
 #undef GTMS_FWD_CL_CASE
 }
 
-template <typename T>
-void launch_backward(int id, const void* y, const void* dy, void* dx, const int32_t* seq_lens, const Geom& g,
-                     float scale, cudaStream_t st)
+template <typename T, int MK>
+void launch_backward_mk(int id, const void* y, const void* dy, void* dx, const int32_t* seq_lens, const Geom& g,
+                        float scale, cudaStream_t st)
 {
     const T* yp = static_cast<const T*>(y);
     const T* gp = static_cast<const T*>(dy);
     T* dp = static_cast<T*>(dx);
 #define GTMS_BWD_VEC_CASE(vid, tw, nv, mb) \
-    case vid: gtms_bwd_vec_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
+    case vid: gtms_bwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
 #define GTMS_BWD_ELEM_CASE(vid, tw, nv) \
-    case kElemBase + vid: gtms_bwd_elem_kernel<T, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
+    case kElemBase + vid: gtms_bwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
 #define GTMS_BWD_CL_CASE(vid, cl, tw, nv, mb) \
-    case kClusterBase + vid: gtms_bwd_cluster_kernel<T, cl, tw, nv, mb><<<cluster_grid_for<cl>(g.rows), tw, 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
+    case kClusterBase + vid: gtms_bwd_cluster_kernel<T, MK, cl, tw, nv, mb><<<cluster_grid_for<cl>(g.rows), tw, 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
     if constexpr (sizeof(T) == 4) {
         switch (id) { GTMS_BWD_VEC4(GTMS_BWD_VEC_CASE) GTMS_ELEM(GTMS_BWD_ELEM_CASE) GTMS_BWD_CL4(GTMS_BWD_CL_CASE) default: break; }
     } else {
@@ -73,6 +73,21 @@ void launch_backward(int id, const void* y, const void* dy, void* dx, const int3
 #undef GTMS_BWD_VEC_CASE
 #undef GTMS_BWD_ELEM_CASE
 #undef GTMS_BWD_CL_CASE
+}
+
+// One translation unit instantiates one mask kind of one dtype and direction.
+template <typename T, int MK>
+void launch_forward(int id, const void* x, void* y, const int32_t* seq_lens, const Geom& g, float scale,
+                    cudaStream_t st)
+{
+    launch_forward_mk<T, MK>(id, x, y, seq_lens, g, scale, st);
+}
+
+template <typename T, int MK>
+void launch_backward(int id, const void* y, const void* dy, void* dx, const int32_t* seq_lens, const Geom& g,
+                     float scale, cudaStream_t st)
+{
+    launch_backward_mk<T, MK>(id, y, dy, dx, seq_lens, g, scale, st);
 }
 
 }  // namespace gtms

@@ -65,6 +65,10 @@ def _load():
             lib.gtms_oracle_backward_masked.argtypes = [vp, vp, ci, vp, i64, i64, i64, dp, ci, i64, i64, i64, vp]
             lib.gtms_oracle_forward_masked.restype = ctypes.c_int
             lib.gtms_oracle_backward_masked.restype = ctypes.c_int
+            lib.gtms_oracle_forward_explicit.argtypes = [vp, ci, vp, i64, i64, i64, i64, dp, i64, i64, vp]
+            lib.gtms_oracle_backward_explicit.argtypes = [vp, vp, ci, vp, i64, i64, i64, i64, dp, i64, i64, vp]
+            lib.gtms_oracle_forward_explicit.restype = ctypes.c_int
+            lib.gtms_oracle_backward_explicit.restype = ctypes.c_int
             lib.gtms_oracle_round.argtypes = [vp, i64, ctypes.c_int, vp]
             lib.gtms_oracle_decode.argtypes = [vp, i64, ctypes.c_int, vp]
             for f in (lib.gtms_oracle_forward, lib.gtms_oracle_backward,
@@ -144,6 +148,49 @@ def backward(y, dy, seq_lens, B, M, S, scale, dtype, row_begin=0, row_end=None, 
     row_end = B * M * S if row_end is None else row_end
     return _run_rows("gtms_oracle_backward_masked", [y, dy], dtype, seq_lens, B, M, S, scale,
                      row_begin, row_end, threads, mask=(mask_kind, window))
+
+
+def _run_explicit(kernel, ins, dtype, mask, B, M, S, scale, row_begin, row_end, threads):
+    lib = _load()
+    mk = np.ascontiguousarray(mask, dtype=np.uint8)
+    if mk.ndim != 3 or mk.shape[1:] != (S, S) or mk.shape[0] not in (1, B):
+        raise ValueError("mask must be uint8 [1 or B, S, S]")
+    rows = row_end - row_begin
+    out = np.empty((rows, S), dtype=np.float64)
+    arrs = [_as_bits(a, dtype).reshape(-1) for a in ins]
+    eb = _ELEM_BYTES[dtype]
+
+    def work(chunk):
+        r0, r1 = chunk
+        off = (r0 - row_begin) * S
+        ptrs = [ctypes.c_void_p(a.ctypes.data + off * eb) for a in arrs]
+        rc = getattr(lib, kernel)(*ptrs, dtype, mk.ctypes.data, mk.shape[0], B, M, S, float(scale), r0, r1,
+                                  ctypes.c_void_p(out.ctypes.data + off * 8))
+        if rc != 0:
+            raise ValueError(f"{kernel} rejected its arguments")
+
+    chunks = _row_chunks(row_begin, row_end, threads)
+    if len(chunks) == 1:
+        work(chunks[0])
+    else:
+        with _cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(work, chunks))
+    return out
+
+
+def forward_explicit(x, mask, B, M, S, scale, dtype, row_begin=0, row_end=None, threads=1):
+    """Softmax of scale*x over the entries whose mask byte is nonzero ("优化ScaledMaskSoftmax算子",
+    sections 2.2 / 3.1 / 4.1); ``mask`` uint8 [1 or B, S, S], shared by the heads. Float64 [rows, S]."""
+    row_end = B * M * S if row_end is None else row_end
+    return _run_explicit("gtms_oracle_forward_explicit", [x], dtype, mask, B, M, S, scale, row_begin, row_end,
+                         threads)
+
+
+def backward_explicit(y, dy, mask, B, M, S, scale, dtype, row_begin=0, row_end=None, threads=1):
+    """Backward of forward_explicit: dx = scale*y*(dy - rowsum(dy*y)) on kept entries, 0 elsewhere."""
+    row_end = B * M * S if row_end is None else row_end
+    return _run_explicit("gtms_oracle_backward_explicit", [y, dy], dtype, mask, B, M, S, scale, row_begin, row_end,
+                         threads)
 
 
 def round_to(values, dtype: int) -> np.ndarray:

@@ -46,6 +46,14 @@
  * of width w. Reading taken for kind 1: padded query rows stay all-zero, as in
  * the default op.
  *
+ * Explicit mask ("优化ScaledMaskSoftmax算子", sections 2.2 and 3.1: the op takes
+ * the input, a mask tensor and the scale). Reading taken: a nonzero mask byte
+ * marks a kept entry -- the article's own masks are ones(L, L).tril(...) and
+ * arange(L) < lengths, both 1 where attention is allowed -- and a row with no
+ * kept entry is all +0.0 (section 4.1 guards the all-masked row). The mask is
+ * uint8 [mask_batches, S, S] with mask_batches 1 (one mask for every batch) or
+ * B, and is shared by the M heads.
+ *
  * Build: cc -O2 -fno-fast-math -fPIC -shared gtms_oracle.c -o libgtms_oracle.so -lm
  */
 #include <math.h>
@@ -299,6 +307,75 @@ int gtms_oracle_backward(const void* y, const void* dy, int dtype, const int32_t
                          int64_t row_begin, int64_t row_end, double* dx)
 {
     return gtms_oracle_backward_masked(y, dy, dtype, seq_lens, B, M, S, scale, 0, 0, row_begin, row_end, dx);
+}
+
+/* ---- explicit mask ---- */
+
+static const uint8_t* mask_row(const uint8_t* mask, int64_t mask_batches, int64_t M, int64_t S, int64_t q)
+{
+    const int64_t b = mask_batches == 1 ? 0 : q / (M * S);
+    return mask + (b * S + q % S) * S;
+}
+
+int gtms_oracle_forward_explicit(const void* x, int dtype, const uint8_t* mask, int64_t mask_batches,
+                                 int64_t B, int64_t M, int64_t S, double scale,
+                                 int64_t row_begin, int64_t row_end, double* y)
+{
+    if (dtype < ORC_F32 || dtype > ORC_F64 || bad_shape(B, M, S, row_begin, row_end) ||
+        (mask_batches != 1 && mask_batches != B))
+        return ORC_BAD_ARG;
+    for (int64_t q = row_begin; q < row_end; ++q) {
+        const int64_t base = (q - row_begin) * S;
+        const uint8_t* keep = mask_row(mask, mask_batches, M, S, q);
+        double* yr = y + base;
+        double zmax = -INFINITY;
+        int any = 0;
+        for (int64_t c = 0; c < S; ++c) {
+            yr[c] = 0.0;
+            if (keep[c]) {
+                const double z = scale * load_elem(x, base + c, dtype);
+                if (!any || z > zmax)
+                    zmax = z;
+                any = 1;
+            }
+        }
+        if (!any)
+            continue;
+        double sum = 0.0;
+        for (int64_t c = 0; c < S; ++c)
+            if (keep[c]) {
+                yr[c] = exp(scale * load_elem(x, base + c, dtype) - zmax);
+                sum += yr[c];
+            }
+        for (int64_t c = 0; c < S; ++c)
+            if (keep[c])
+                yr[c] = yr[c] / sum;
+    }
+    return ORC_OK;
+}
+
+int gtms_oracle_backward_explicit(const void* y, const void* dy, int dtype, const uint8_t* mask,
+                                  int64_t mask_batches, int64_t B, int64_t M, int64_t S, double scale,
+                                  int64_t row_begin, int64_t row_end, double* dx)
+{
+    if (dtype < ORC_F32 || dtype > ORC_F64 || bad_shape(B, M, S, row_begin, row_end) ||
+        (mask_batches != 1 && mask_batches != B))
+        return ORC_BAD_ARG;
+    for (int64_t q = row_begin; q < row_end; ++q) {
+        const int64_t base = (q - row_begin) * S;
+        const uint8_t* keep = mask_row(mask, mask_batches, M, S, q);
+        double* dxr = dx + base;
+        double dot = 0.0;
+        for (int64_t c = 0; c < S; ++c) {
+            dxr[c] = 0.0;
+            if (keep[c])
+                dot += load_elem(dy, base + c, dtype) * load_elem(y, base + c, dtype);
+        }
+        for (int64_t c = 0; c < S; ++c)
+            if (keep[c])
+                dxr[c] = scale * load_elem(y, base + c, dtype) * (load_elem(dy, base + c, dtype) - dot);
+    }
+    return ORC_OK;
 }
 
 /* ---- element conversion helpers (used by the tests to form expected bits) ---- */

@@ -71,10 +71,12 @@ class Stats:
         return self.bad_masked == 0 and self.bad_live == 0
 
 
-def compare_rows(gpu_bits: np.ndarray, ref: np.ndarray, kept: np.ndarray, dtype: str, stats: Stats):
-    """gpu_bits [rows, S] raw bits, ref [rows, S] float64 oracle, kept [rows] kept-prefix lengths."""
+def compare_rows(gpu_bits: np.ndarray, ref: np.ndarray, kept, dtype: str, stats: Stats):
+    """gpu_bits [rows, S] raw bits, ref [rows, S] float64 oracle, kept = (c0, c1) kept column range per row."""
     S = gpu_bits.shape[1]
-    live = np.arange(S)[None, :] < kept[:, None]
+    c0, c1 = kept
+    col = np.arange(S)[None, :]
+    live = (col >= c0[:, None]) & (col < c1[:, None])
     stats.live += int(live.sum())
     stats.masked += int((~live).sum())
     stats.bad_masked += int(np.count_nonzero(gpu_bits[~live]))
@@ -97,23 +99,29 @@ def compare_rows(gpu_bits: np.ndarray, ref: np.ndarray, kept: np.ndarray, dtype:
         stats.bad_live += int(np.count_nonzero(ulp > HALF_ULP_TOL))
 
 
-def kept_for_rows(seq_lens: np.ndarray, M: int, S: int, q0: int, q1: int) -> np.ndarray:
-    n = oracle.kept_prefix_lengths(seq_lens, M, S)          # [B, S]
+def kept_for_rows(seq_lens: np.ndarray, M: int, S: int, q0: int, q1: int, mask_kind=0, window=0):
+    """(c0, c1) kept column range of each row q in [q0, q1)."""
+    c0, c1 = oracle.kept_ranges(seq_lens, S, mask_kind, window)          # [B, S]
     q = np.arange(q0, q1)
-    return n[q // (M * S), q % S]
+    b, r = q // (M * S), q % S
+    return c0[b, r], c1[b, r]
 
 
-def check_forward(x_bits_rows, y_bits_rows, seq_lens, B, M, S, scale, dtype, q0, q1, stats, threads=8):
+def check_forward(x_bits_rows, y_bits_rows, seq_lens, B, M, S, scale, dtype, q0, q1, stats, threads=8,
+                  mask_kind=0, window=0):
     """Oracle forward on rows [q0, q1) (x given as raw bits) vs the GPU's y bits."""
-    ref = oracle.forward(x_bits_rows, seq_lens, B, M, S, scale, si.DTYPE_CODES[dtype], q0, q1, threads=threads)
-    compare_rows(y_bits_rows.reshape(q1 - q0, S), ref, kept_for_rows(seq_lens, M, S, q0, q1), dtype, stats)
+    ref = oracle.forward(x_bits_rows, seq_lens, B, M, S, scale, si.DTYPE_CODES[dtype], q0, q1, threads=threads,
+                         mask_kind=mask_kind, window=window)
+    compare_rows(y_bits_rows.reshape(q1 - q0, S), ref, kept_for_rows(seq_lens, M, S, q0, q1, mask_kind, window),
+                 dtype, stats)
 
 
 def check_backward(y_bits_rows, dy_bits_rows, dx_bits_rows, seq_lens, B, M, S, scale, dtype, q0, q1, stats,
-                   threads=8):
+                   threads=8, mask_kind=0, window=0):
     ref = oracle.backward(y_bits_rows, dy_bits_rows, seq_lens, B, M, S, scale, si.DTYPE_CODES[dtype], q0, q1,
-                          threads=threads)
-    compare_rows(dx_bits_rows.reshape(q1 - q0, S), ref, kept_for_rows(seq_lens, M, S, q0, q1), dtype, stats)
+                          threads=threads, mask_kind=mask_kind, window=window)
+    compare_rows(dx_bits_rows.reshape(q1 - q0, S), ref, kept_for_rows(seq_lens, M, S, q0, q1, mask_kind, window),
+                 dtype, stats)
 
 
 def row_chunks(q0: int, q1: int, S: int, max_elems: int = 1 << 23):
@@ -122,18 +130,19 @@ def row_chunks(q0: int, q1: int, S: int, max_elems: int = 1 << 23):
         yield a, min(q1, a + step)
 
 
-def oracle_forward_bits(x_bits: np.ndarray, seq_lens, B, M, S, scale, dtype, threads=8) -> np.ndarray:
+def oracle_forward_bits(x_bits: np.ndarray, seq_lens, B, M, S, scale, dtype, threads=8, mask_kind=0,
+                        window=0) -> np.ndarray:
     """Oracle forward of a whole small tensor, rounded once to the IO dtype (raw bits)."""
     out = np.empty(B * M * S * S, dtype=_NP_BITS[dtype])
     flat = x_bits.reshape(-1)
     for a, b in row_chunks(0, B * M * S, S):
         ref = oracle.forward(flat[a * S:b * S], seq_lens, B, M, S, scale, si.DTYPE_CODES[dtype], a, b,
-                             threads=threads)
+                             threads=threads, mask_kind=mask_kind, window=window)
         out[a * S:b * S] = oracle.round_to(ref, si.DTYPE_CODES[dtype]).reshape(-1)
     return out.reshape(B, M, S, S)
 
 
-def masked_bits_all_zero(out: torch.Tensor, seq_lens_dev: torch.Tensor, dtype: str) -> bool:
+def masked_bits_all_zero(out: torch.Tensor, seq_lens_dev: torch.Tensor, dtype: str, mask_kind=0, window=0) -> bool:
     """On the device, for every row of every batch: no masked element has a nonzero bit."""
     B, M, S, _ = out.shape
     bits = out.view(_BITS[dtype])
@@ -141,7 +150,12 @@ def masked_bits_all_zero(out: torch.Tensor, seq_lens_dev: torch.Tensor, dtype: s
     row = torch.arange(S, device=out.device)
     for b in range(B):
         L = int(seq_lens_dev[b].clamp(0, S).item())
-        kept = (col[None, :] <= row[:, None]) & (row[:, None] < L)
+        if mask_kind == 1:
+            kept = (col[None, :] < L) & (row[:, None] < L)
+        else:
+            kept = (col[None, :] <= row[:, None]) & (row[:, None] < L)
+            if mask_kind == 2:
+                kept &= col[None, :] > row[:, None] - window
         if bool(((bits[b] != 0) & ~kept).any().item()):
             return False
     return True

@@ -123,6 +123,16 @@ def test_shape_and_scale_errors(lib, call):
     assert call(B=1 << 30, M=1 << 30, S=4096) == INVALID
 
 
+def test_mask_arguments(lib):
+    for fn, ptrs in ((gtms.gtms_forward_masked, (X, Y, LENS)), (gtms.gtms_backward_masked, (X, DY, Y, LENS))):
+        assert fn(*ptrs, 2, 3, 64, 1.0, 3, 0, F32, None) == UNSUPPORTED      # unknown mask kind
+        assert fn(*ptrs, 2, 3, 64, 1.0, -1, 0, F32, None) == UNSUPPORTED
+        assert fn(*ptrs, 2, 3, 64, 1.0, 2, 0, F32, None) == INVALID          # window must be >= 1
+        assert fn(*ptrs, 2, 3, 64, 1.0, 2, -4, F32, None) == INVALID
+        assert fn(*ptrs, 0, 3, 64, 1.0, 2, 4, F32, None) == OK               # empty work
+        assert fn(*ptrs, 2, 3, 64, float("nan"), 1, 0, F32, None) == INVALID
+
+
 @pytest.mark.parametrize("call", [fwd, bwd])
 def test_long_rows_need_16_byte_units(lib, call):
     assert call(S=8193) == UNSUPPORTED                  # fp32 row of 32772 bytes

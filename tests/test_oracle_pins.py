@@ -479,3 +479,72 @@ def test_kept_ranges_match_oracle_zero_pattern(kind, w):
     col = np.arange(S)[None, None, :]
     kept = (col >= c0[:, :, None]) & (col < c1[:, :, None])
     assert np.array_equal(y[:, 0] != 0.0, kept)
+
+
+# ---------------------------------------------------------------------------
+# Explicit mask ("优化ScaledMaskSoftmax算子" sections 2.2 / 3.1 / 4.1)
+# ---------------------------------------------------------------------------
+
+def _fwd64_explicit(x, mask, scale=1.0):
+    B, M, S, _ = x.shape
+    return oracle.forward_explicit(np.ascontiguousarray(x, np.float64), mask, B, M, S, scale, F64).reshape(B, M, S, S)
+
+
+def _bwd64_explicit(y, dy, mask, scale=1.0):
+    B, M, S, _ = y.shape
+    return oracle.backward_explicit(np.ascontiguousarray(y, np.float64), np.ascontiguousarray(dy, np.float64), mask,
+                                    B, M, S, scale, F64).reshape(B, M, S, S)
+
+
+def test_explicit_mask_matches_torch_masked_softmax():
+    """Random keep-mask with some all-masked rows: torch softmax of a -inf-filled
+    input (NaN rows of all-masked inputs become 0, as the section 4.1 guard does)."""
+    g = torch.Generator().manual_seed(400)
+    B, M, S = 3, 2, 19
+    x = torch.randn(B, M, S, S, generator=g, dtype=torch.float64) * 2
+    keep = torch.rand(B, S, S, generator=g) < 0.4
+    keep[:, 3, :] = False
+    keep[1, 7, :] = True
+    ref = torch.nan_to_num(torch.softmax((x * 0.8).masked_fill(~keep[:, None], float("-inf")), dim=-1), nan=0.0)
+    y = _fwd64_explicit(x.numpy(), keep.numpy().astype(np.uint8), 0.8)
+    np.testing.assert_allclose(y, ref.numpy(), rtol=0, atol=1e-15)
+    assert np.all(y[:, :, 3, :] == 0.0)
+
+
+def test_explicit_mask_reduces_to_the_grouped_families():
+    """A tril keep-mask restricted to r, c < L is the grouped-tril op; a length
+    mask is kind 1; one [1, S, S] mask broadcasts over the batches."""
+    rng = np.random.default_rng(22)
+    B, M, S = 3, 2, 14
+    x = rng.standard_normal((B, M, S, S)) * 2
+    sl = np.array([14, 9, 0], np.int32)
+    r, c = np.arange(S)[:, None], np.arange(S)[None, :]
+    tril = np.stack([((c <= r) & (r < L)) for L in sl]).astype(np.uint8)
+    length = np.stack([((c < L) & (r < L)) for L in sl]).astype(np.uint8)
+    assert np.array_equal(_fwd64_explicit(x, tril, 0.5), _fwd64(x, sl, 0.5))
+    assert np.array_equal(_fwd64_explicit(x, length, 0.5), _fwd64_kind(x, sl, 0.5, 1))
+    one = (c <= r).astype(np.uint8)[None]
+    assert np.array_equal(_fwd64_explicit(x, one, 0.5), _fwd64(x, np.array([S, S, S], np.int32), 0.5))
+    with pytest.raises(ValueError):
+        _fwd64_explicit(x, np.ones((2, S, S), np.uint8))
+
+
+def test_explicit_mask_backward_matches_central_differences():
+    rng = np.random.default_rng(23)
+    S, scale, h = 6, 0.9, 1e-6
+    x = rng.standard_normal((1, 1, S, S))
+    dy = rng.standard_normal((1, 1, S, S))
+    keep = (rng.random((1, S, S)) < 0.5).astype(np.uint8)
+    keep[0, 2, :] = 0
+    y = _fwd64_explicit(x, keep, scale)
+    dx = _bwd64_explicit(y, dy, keep, scale)
+    num = np.zeros_like(x)
+    for r in range(S):
+        for c in range(S):
+            xp, xm = x.copy(), x.copy()
+            xp[0, 0, r, c] += h
+            xm[0, 0, r, c] -= h
+            num[0, 0, r, c] = ((_fwd64_explicit(xp, keep, scale) * dy).sum()
+                               - (_fwd64_explicit(xm, keep, scale) * dy).sum()) / (2 * h)
+    np.testing.assert_allclose(dx, num, rtol=0, atol=1e-8)
+    assert np.all(dx[0, 0][keep[0] == 0] == 0.0)

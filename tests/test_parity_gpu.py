@@ -32,8 +32,9 @@ def _lens_dev(w, dev):
     return torch.from_numpy(si.seq_lens(w)).to(dev)
 
 
-def run_and_check(w, dev, backward=True, x_cpu=None, offset_elems=0):
+def run_and_check(w, dev, backward=True, x_cpu=None, offset_elems=0, mask_kind=0, window=0):
     """Full element-wise parity of forward (and backward) for a small workload."""
+    mk = dict(mask_kind=mask_kind, window=window)
     B, M, S = w.B, w.M, w.S
     lens = si.seq_lens(w)
     lens_d = torch.from_numpy(lens).to(dev)
@@ -49,28 +50,28 @@ def run_and_check(w, dev, backward=True, x_cpu=None, offset_elems=0):
         return view
 
     y = place(torch.zeros_like(x))
-    gtms.forward(place(x), lens_d, w.scale, out=y)
+    gtms.forward(place(x), lens_d, w.scale, out=y, **mk)
     torch.cuda.synchronize()
     y_bits = to_bits(y, w.dtype).reshape(-1)
     st = Stats()
     for a, b in row_chunks(0, w.rows, S):
-        check_forward(x_bits[a * S:b * S], y_bits[a * S:b * S], lens, B, M, S, w.scale, w.dtype, a, b, st)
-    assert st.ok, f"forward {w.describe()}: {st}"
+        check_forward(x_bits[a * S:b * S], y_bits[a * S:b * S], lens, B, M, S, w.scale, w.dtype, a, b, st, **mk)
+    assert st.ok, f"forward {w.describe()} {mk}: {st}"
     if not backward:
         return st, None
-    y_or = oracle_forward_bits(x_bits, lens, B, M, S, w.scale, w.dtype)
+    y_or = oracle_forward_bits(x_bits, lens, B, M, S, w.scale, w.dtype, **mk)
     dy = si.make_dy(w, "cpu")
     dy_bits = to_bits(dy, w.dtype).reshape(-1)
     dx = place(torch.zeros_like(dy))
-    gtms.backward(place(from_bits(y_or, w.dtype, "cpu")), place(dy), lens_d, w.scale, out=dx)
+    gtms.backward(place(from_bits(y_or, w.dtype, "cpu")), place(dy), lens_d, w.scale, out=dx, **mk)
     torch.cuda.synchronize()
     dx_bits = to_bits(dx, w.dtype).reshape(-1)
     yb = y_or.reshape(-1)
     sb = Stats()
     for a, b in row_chunks(0, w.rows, S):
         check_backward(yb[a * S:b * S], dy_bits[a * S:b * S], dx_bits[a * S:b * S], lens, B, M, S, w.scale,
-                       w.dtype, a, b, sb)
-    assert sb.ok, f"backward {w.describe()}: {sb}"
+                       w.dtype, a, b, sb, **mk)
+    assert sb.ok, f"backward {w.describe()} {mk}: {sb}"
     return st, sb
 
 
@@ -418,3 +419,57 @@ def test_host_resident_buffers_match_device_calls(dev):
     dx_h = gtms.backward_host(y_h, dy_h, lens_h, 1.0, device=dev)
     torch.cuda.synchronize()
     assert torch.equal(y_h, y_ref.cpu()) and torch.equal(dx_h, dx_ref.cpu())
+
+
+# ---------------------------------------------------------------------------
+# Mask families ("优化ScaledMaskSoftmax算子" section 6): length mask, sliding window
+# ---------------------------------------------------------------------------
+
+MASK_CASES = [
+    (1, 0, 1000, "f32"), (1, 0, 2048, "bf16"), (1, 0, 37, "f16"), (1, 0, 8192, "f16"), (1, 0, 16384, "bf16"),
+    (2, 1, 1000, "f32"), (2, 7, 1000, "f32"), (2, 100, 2048, "bf16"), (2, 257, 33, "f16"), (2, 300, 8192, "f16"),
+    (2, 5000, 16384, "f32"), (2, 8, 64, "bf16"), (2, 9, 5, "f32"),
+]
+
+
+@pytest.mark.parametrize("kind,window,S,dtype", MASK_CASES)
+def test_mask_families(dev, kind, window, S, dtype):
+    """Length mask and sliding causal window: every element, head and tail partial units, per-row and
+    cluster kernels, 16-byte and element paths."""
+    M = 2 if S <= 2048 else 1
+    w = si.custom(f"mask{kind}_{S}", 4, M, S, dtype, 0.125 if dtype != "f32" else 1.0,
+                  seq_lens=(S, S // 2 + 3, 1, 0), x_std=2.0, seed=S + 31 * kind + window)
+    run_and_check(w, dev, mask_kind=kind, window=window)
+
+
+def test_mask_family_sentinels_and_aliasing(dev):
+    """Masked inputs of the window family are never read; in-place works."""
+    S, win = 1000, 33
+    w = si.custom("winsent", 2, 2, S, "f32", 1.0, seq_lens=(S, 500), seed=33)
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    c0, c1 = oracle.kept_ranges(lens, S, 2, win)
+    col = torch.arange(S, device=dev)
+    kept = ((col[None, None, :] >= torch.from_numpy(c0).to(dev)[:, :, None])
+            & (col[None, None, :] < torch.from_numpy(c1).to(dev)[:, :, None]))[:, None]
+    x = si.make_x(w, dev)
+    ref = gtms.forward(x, lens_d, 1.0, mask_kind=2, window=win)
+    y = gtms.forward(torch.where(kept, x, float("nan")), lens_d, 1.0, mask_kind=2, window=win)
+    xi = x.clone()
+    gtms.forward(xi, lens_d, 1.0, out=xi, mask_kind=2, window=win)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref) and torch.equal(xi, ref)
+    assert masked_bits_all_zero(ref, lens_d, "f32", mask_kind=2, window=win)
+
+
+def test_wide_window_equals_default_op(dev):
+    w = si.custom("widewin", 2, 2, 1000, "f32", 1.0, seq_lens=(1000, 700), seed=34)
+    lens_d = _lens_dev(w, dev)
+    x = si.make_x(w, dev)
+    dy = si.make_dy(w, dev)
+    y0 = gtms.forward(x, lens_d)
+    y2 = gtms.forward(x, lens_d, mask_kind=2, window=1000)
+    d0 = gtms.backward(y0, dy, lens_d)
+    d2 = gtms.backward(y0, dy, lens_d, mask_kind=2, window=5000)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y2) and torch.equal(d0, d2)
