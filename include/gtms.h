@@ -139,6 +139,27 @@ int gtms_forward_masked(const void* x, void* y, const int32_t* seq_lens, int64_t
 int gtms_backward_masked(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B, int64_t M,
                          int64_t S, float scale, int mask_kind, int64_t window, int dtype, void* stream);
 
+/*
+ * Masked softmax with an explicit keep mask ("优化ScaledMaskSoftmax算子",
+ * sections 2.2 and 3.1: input, mask, scale; section 4.1: a row with nothing
+ * kept is zero). y[b, m, r, c] = softmax over {c' : mask[b', r, c'] != 0} of
+ * scale * x[b, m, r, c'] at kept entries, +0.0 elsewhere; b' = 0 when
+ * mask_batches == 1, else b. The backward is dx = scale * y * (dy - rowsum(dy * y))
+ * over the same kept set.
+ *   mask         device uint8 [mask_batches, S, S], 8-byte aligned, read-only,
+ *                shared by the M heads; nonzero = keep.
+ *   mask_batches 1 or B.
+ * Masked inputs are not loaded: each 16-byte unit of x (or of y and dy) is
+ * read only if its mask bytes keep at least one element.
+ * GTMS_ERR_INVALID_ARG also covers a null or misaligned mask, mask_batches
+ * other than 1 or B, and a mask overlapping the output. GTMS_ERR_UNSUPPORTED:
+ * S > 8192, rows that are not 16-byte multiples, or buffers not 16-byte aligned.
+ */
+int gtms_forward_explicit(const void* x, void* y, const uint8_t* mask, int64_t mask_batches, int64_t B, int64_t M,
+                          int64_t S, float scale, int dtype, void* stream);
+int gtms_backward_explicit(const void* y, const void* dy, void* dx, const uint8_t* mask, int64_t mask_batches,
+                           int64_t B, int64_t M, int64_t S, float scale, int dtype, void* stream);
+
 /* Static, NUL-terminated name of a status code ("GTMS_OK", ...). */
 const char* gtms_status_string(int status);
 

@@ -28,7 +28,7 @@ GTMS_MASK_GROUPED_TRIL, GTMS_MASK_LENGTH, GTMS_MASK_SLIDING_WINDOW = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gtms_forward", "gtms_backward", "gtms_status_string", "gtms_version",
                     "gtms_kernel_name", "gtms_device_pointer_of_host", "gtms_forward_masked",
-                    "gtms_backward_masked")
+                    "gtms_backward_masked", "gtms_forward_explicit", "gtms_backward_explicit")
 
 _lib = None
 _lock = threading.Lock()
@@ -65,6 +65,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.gtms_backward_masked.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, i64,
                                              ctypes.c_int, vp]
         lib.gtms_backward_masked.restype = ctypes.c_int
+        lib.gtms_forward_explicit.argtypes = [vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
+        lib.gtms_forward_explicit.restype = ctypes.c_int
+        lib.gtms_backward_explicit.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
+        lib.gtms_backward_explicit.restype = ctypes.c_int
         lib.gtms_status_string.argtypes = [ctypes.c_int]
         lib.gtms_status_string.restype = ctypes.c_char_p
         lib.gtms_version.argtypes = []
@@ -96,6 +100,14 @@ def gtms_forward_masked(x, y, seq_lens, B, M, S, scale, mask_kind, window, dtype
 
 def gtms_backward_masked(y, dy, dx, seq_lens, B, M, S, scale, mask_kind, window, dtype, stream) -> int:
     return load_library().gtms_backward_masked(y, dy, dx, seq_lens, B, M, S, scale, mask_kind, window, dtype, stream)
+
+
+def gtms_forward_explicit(x, y, mask, mask_batches, B, M, S, scale, dtype, stream) -> int:
+    return load_library().gtms_forward_explicit(x, y, mask, mask_batches, B, M, S, scale, dtype, stream)
+
+
+def gtms_backward_explicit(y, dy, dx, mask, mask_batches, B, M, S, scale, dtype, stream) -> int:
+    return load_library().gtms_backward_explicit(y, dy, dx, mask, mask_batches, B, M, S, scale, dtype, stream)
 
 
 def status_string(status: int) -> str:
@@ -186,6 +198,54 @@ def backward(y, dy, seq_lens, scale: float = 1.0, out=None, mask_kind: int = GTM
                               float(scale), int(mask_kind), int(window), _dtype_code(y), stream)
     if rc != GTMS_OK:
         raise GtmsError("gtms_backward_masked", rc)
+    return dx
+
+
+def _check_mask(mask, B, S, device):
+    import torch
+
+    if mask.dtype != torch.uint8 or mask.dim() != 3 or mask.shape[1:] != (S, S) or mask.shape[0] not in (1, B) \
+            or mask.device != device or not mask.is_contiguous():
+        raise ValueError("mask must be a contiguous uint8 CUDA tensor [1 or B, S, S] on the scores' device")
+
+
+def forward_explicit(x, mask, scale: float = 1.0, out=None):
+    """Softmax of scale * x over the entries whose mask byte is nonzero (mask uint8 [1 or B, S, S],
+    shared by the heads); +0.0 elsewhere, all-masked rows zero. ``out`` may be ``x``."""
+    import torch
+
+    _check_scores("x", x)
+    B, M, S, _ = x.shape
+    _check_mask(mask, B, S, x.device)
+    y = torch.empty_like(x) if out is None else out
+    if y.shape != x.shape or y.dtype != x.dtype or y.device != x.device or not y.is_contiguous():
+        raise ValueError("out must match x in shape, dtype, device and be contiguous")
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    rc = gtms_forward_explicit(x.data_ptr(), y.data_ptr(), mask.data_ptr(), mask.shape[0], B, M, S, float(scale),
+                               _dtype_code(x), stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_forward_explicit", rc)
+    return y
+
+
+def backward_explicit(y, dy, mask, scale: float = 1.0, out=None):
+    """Backward of forward_explicit over the same kept entries; ``out`` may be ``y`` or ``dy``."""
+    import torch
+
+    _check_scores("y", y)
+    _check_scores("dy", dy)
+    if dy.shape != y.shape or dy.dtype != y.dtype or dy.device != y.device:
+        raise ValueError("dy must match y in shape, dtype and device")
+    B, M, S, _ = y.shape
+    _check_mask(mask, B, S, y.device)
+    dx = torch.empty_like(y) if out is None else out
+    if dx.shape != y.shape or dx.dtype != y.dtype or dx.device != y.device or not dx.is_contiguous():
+        raise ValueError("out must match y in shape, dtype, device and be contiguous")
+    stream = torch.cuda.current_stream(y.device).cuda_stream
+    rc = gtms_backward_explicit(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), mask.data_ptr(), mask.shape[0], B, M, S,
+                                float(scale), _dtype_code(y), stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_backward_explicit", rc)
     return dx
 
 

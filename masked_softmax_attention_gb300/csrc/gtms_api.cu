@@ -34,6 +34,20 @@ GTMS_EXTERN_FOR(__half, 0)
 GTMS_EXTERN_FOR(__half, 1)
 GTMS_EXTERN_FOR(__half, 2)
 #undef GTMS_EXTERN_FOR
+template <typename T>
+void launch_forward_explicit(int, const void*, void*, const uint8_t*, int32_t, const Geom&, float, cudaStream_t);
+template <typename T>
+void launch_backward_explicit(int, const void*, const void*, void*, const uint8_t*, int32_t, const Geom&, float,
+                              cudaStream_t);
+#define GTMS_EXTERN_EXPLICIT(T)                                                                                     \
+    extern template void launch_forward_explicit<T>(int, const void*, void*, const uint8_t*, int32_t, const Geom&, \
+                                                    float, cudaStream_t);                                          \
+    extern template void launch_backward_explicit<T>(int, const void*, const void*, void*, const uint8_t*, int32_t, \
+                                                     const Geom&, float, cudaStream_t);
+GTMS_EXTERN_EXPLICIT(float)
+GTMS_EXTERN_EXPLICIT(__nv_bfloat16)
+GTMS_EXTERN_EXPLICIT(__half)
+#undef GTMS_EXTERN_EXPLICIT
 }  // namespace gtms
 
 namespace {
@@ -220,6 +234,75 @@ GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int
                               int64_t S, float scale, int dtype, void* stream)
 {
     return gtms_backward_masked(y, dy, dx, seq_lens, B, M, S, scale, GTMS_MASK_GROUPED_TRIL, 0, dtype, stream);
+}
+
+// Shared checks of the explicit-mask entry points: everything gtms_forward
+// checks, plus the mask (non-null, 8-byte aligned, mask_batches 1 or B, no
+// overlap with the output) and the 16-byte row layout the kernels need.
+namespace {
+int check_explicit(const Checked& c, int64_t B, int64_t S, int e, const uint8_t* mask, int64_t mask_batches,
+                   const void* out, bool a16)
+{
+    if (!mask || (mask_batches != 1 && mask_batches != B) || !aligned_to(mask, 8))
+        return GTMS_ERR_INVALID_ARG;
+    const uint64_t mask_bytes = static_cast<uint64_t>(mask_batches) * S * S;
+    if (overlaps(out, c.bytes, mask, mask_bytes))
+        return GTMS_ERR_INVALID_ARG;
+    if (!a16 || (S * e) % 16 != 0 || S > 8192)
+        return GTMS_ERR_UNSUPPORTED;
+    return GTMS_OK;
+}
+}  // namespace
+
+GTMS_EXPORT int gtms_forward_explicit(const void* x, void* y, const uint8_t* mask, int64_t mask_batches, int64_t B,
+                                      int64_t M, int64_t S, float scale, int dtype, void* stream)
+{
+    const Checked c = check_shape(B, M, S, scale, dtype);
+    if (c.status != GTMS_OK || c.rows == 0)
+        return c.status;
+    const int e = elem_bytes(dtype);
+    if (!x || !y || !aligned_to(x, e) || !aligned_to(y, e) || bad_alias(y, x, c.bytes))
+        return GTMS_ERR_INVALID_ARG;
+    const int ce = check_explicit(c, B, S, e, mask, mask_batches, y, aligned_to(x, 16) && aligned_to(y, 16));
+    if (ce != GTMS_OK)
+        return ce;
+    const int variant = gtms::pick_variant(0, S, e, true);
+    const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e, 0);
+    const int32_t mb = static_cast<int32_t>(mask_batches);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case GTMS_F32: gtms::launch_forward_explicit<float>(variant, x, y, mask, mb, g, scale, st); break;
+    case GTMS_BF16: gtms::launch_forward_explicit<__nv_bfloat16>(variant, x, y, mask, mb, g, scale, st); break;
+    default: gtms::launch_forward_explicit<__half>(variant, x, y, mask, mb, g, scale, st); break;
+    }
+    return launch_status();
+}
+
+GTMS_EXPORT int gtms_backward_explicit(const void* y, const void* dy, void* dx, const uint8_t* mask,
+                                       int64_t mask_batches, int64_t B, int64_t M, int64_t S, float scale, int dtype,
+                                       void* stream)
+{
+    const Checked c = check_shape(B, M, S, scale, dtype);
+    if (c.status != GTMS_OK || c.rows == 0)
+        return c.status;
+    const int e = elem_bytes(dtype);
+    if (!y || !dy || !dx || !aligned_to(y, e) || !aligned_to(dy, e) || !aligned_to(dx, e) ||
+        bad_alias(dx, y, c.bytes) || bad_alias(dx, dy, c.bytes))
+        return GTMS_ERR_INVALID_ARG;
+    const bool a16 = aligned_to(y, 16) && aligned_to(dy, 16) && aligned_to(dx, 16);
+    const int ce = check_explicit(c, B, S, e, mask, mask_batches, dx, a16);
+    if (ce != GTMS_OK)
+        return ce;
+    const int variant = gtms::pick_variant(1, S, e, true);
+    const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e, 0);
+    const int32_t mb = static_cast<int32_t>(mask_batches);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case GTMS_F32: gtms::launch_backward_explicit<float>(variant, y, dy, dx, mask, mb, g, scale, st); break;
+    case GTMS_BF16: gtms::launch_backward_explicit<__nv_bfloat16>(variant, y, dy, dx, mask, mb, g, scale, st); break;
+    default: gtms::launch_backward_explicit<__half>(variant, y, dy, dx, mask, mb, g, scale, st); break;
+    }
+    return launch_status();
 }
 
 GTMS_EXPORT int gtms_device_pointer_of_host(const void* host, void** device)

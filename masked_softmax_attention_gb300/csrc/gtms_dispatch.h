@@ -6,7 +6,7 @@
 // smallest row capacity first. The forward holds up to 16 (fp32) or 32 (16-bit)
 // kept elements per thread as fp32 exponentials; the backward holds up to 8
 // raw 16-byte units of y and of dy per thread. Rows too long for one warp take a
-// CTA of 64..512 threads. The last number is the minimum number of CTAs per SM
+// CTA of 64..1024 threads, up to 64 KB rows. The last number is the minimum number of CTAs per SM
 // requested from the compiler (__launch_bounds__): it caps registers so that
 // enough rows are in flight per SM. These choices come from a sweep on GB300 of
 // team size, units per thread, register cap and grid shape over the
@@ -16,29 +16,32 @@
 // multiples, and element-aligned buffers, up to S = 8192.
 //
 // Cluster variants serve 16-byte-unit rows longer than the largest CTA variant
-// (32 KB fp32 / 16 KB 16-bit), up to S = 65536: a cluster of 2, 4 or 8 CTAs
-// owns one row (gtms_cluster.cuh).
+// (64 KB: fp32 S > 16384, 16-bit S > 32768), up to S = 65536: a cluster of 2 or
+// 4 CTAs owns one row (gtms_cluster.cuh). Measured on GB300, one 512- or
+// 1024-thread CTA per row beats a cluster for rows that still fit one CTA
+// (S = 16384 bf16: 5.2 vs 3.1 TB/s forward, 6.1 vs 4.3 backward): the
+// cluster barrier per row costs more than the larger CTA's block barriers.
 #pragma once
 
 #include <cstdint>
 
 //                       id  team  units/thread  min CTAs/SM (0: no register cap)
 #define GTMS_FWD_VEC4(X) X(0, 32, 1, 8) X(1, 32, 2, 8) X(2, 32, 4, 8) X(3, 64, 4, 0) \
-                         X(4, 128, 4, 0) X(5, 256, 4, 0) X(6, 512, 4, 0)
+                         X(4, 128, 4, 0) X(5, 256, 4, 0) X(6, 512, 4, 0) X(7, 1024, 4, 0)
 #define GTMS_FWD_VEC2(X) X(0, 32, 1, 8) X(1, 32, 2, 8) X(2, 32, 4, 6) X(3, 64, 4, 16) \
-                         X(4, 128, 4, 8) X(5, 256, 4, 4)
+                         X(4, 128, 4, 8) X(5, 256, 4, 4) X(6, 512, 4, 2) X(7, 1024, 4, 0)
 #define GTMS_BWD_VEC4(X) X(0, 32, 1, 4) X(1, 32, 2, 4) X(2, 32, 4, 4) X(3, 32, 8, 5) \
-                         X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0)
+                         X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0) X(7, 512, 8, 0)
 #define GTMS_BWD_VEC2(X) X(0, 32, 1, 4) X(1, 32, 2, 4) X(2, 32, 4, 4) X(3, 32, 8, 5) \
-                         X(4, 64, 8, 0) X(5, 128, 8, 0)
+                         X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0) X(7, 512, 8, 0)
 //                       id  team  elements/thread
 #define GTMS_ELEM(X) X(0, 32, 1) X(1, 32, 4) X(2, 32, 16) X(3, 32, 32) X(4, 128, 32) X(5, 256, 32)
 // Cluster variants (rows longer than one CTA holds, 16-byte units only):
 //                      id  CTAs/cluster  team  units/thread  min CTAs/SM
-#define GTMS_FWD_CL4(X) X(0, 2, 512, 4, 0) X(1, 4, 512, 4, 0) X(2, 8, 512, 4, 0)
-#define GTMS_FWD_CL2(X) X(0, 2, 256, 4, 0) X(1, 4, 256, 4, 0) X(2, 8, 256, 4, 0)
-#define GTMS_BWD_CL4(X) X(0, 2, 256, 8, 0) X(1, 4, 256, 8, 0) X(2, 8, 256, 8, 0)
-#define GTMS_BWD_CL2(X) X(0, 2, 128, 8, 0) X(1, 4, 128, 8, 0) X(2, 8, 128, 8, 0)
+#define GTMS_FWD_CL4(X) X(0, 2, 1024, 4, 0) X(1, 4, 1024, 4, 0)
+#define GTMS_FWD_CL2(X) X(0, 2, 1024, 4, 0)
+#define GTMS_BWD_CL4(X) X(0, 2, 512, 8, 0) X(1, 4, 512, 8, 0)
+#define GTMS_BWD_CL2(X) X(0, 2, 512, 8, 0)
 
 namespace gtms {
 

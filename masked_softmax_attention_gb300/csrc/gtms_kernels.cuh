@@ -266,6 +266,14 @@ template <> struct Pairs<float> {
             if (e < lo || e >= hi)
                 u.w[e] = 0u;
     }
+    // Zero the raw bits of elements whose keep bit is 0.
+    __device__ static void clear_unkept(Unit16& u, uint32_t keep)
+    {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (!(keep & (1u << e)))
+                u.w[e] = 0u;
+    }
 };
 
 template <> struct Pairs<__nv_bfloat16> {
@@ -287,6 +295,13 @@ template <> struct Pairs<__nv_bfloat16> {
             if (e < lo || e >= hi)
                 u.w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
     }
+    __device__ static void clear_unkept(Unit16& u, uint32_t keep)
+    {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (!(keep & (1u << e)))
+                u.w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
+    }
 };
 
 template <> struct Pairs<__half> {
@@ -306,6 +321,13 @@ template <> struct Pairs<__half> {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             if (e < lo || e >= hi)
+                u.w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
+    }
+    __device__ static void clear_unkept(Unit16& u, uint32_t keep)
+    {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (!(keep & (1u << e)))
                 u.w[e >> 1] &= (e & 1) ? 0x0000ffffu : 0xffff0000u;
     }
 };

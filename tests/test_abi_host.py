@@ -89,9 +89,12 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name(0, 1000, F32, aligned16=False) == "gtms_fwd_elem_kernel<f32,team32,x32>"
     assert gtms.kernel_name(1, 8191, F16) == "gtms_bwd_elem_kernel<f16,team256,x32>"
     # rows longer than one CTA holds: a cluster of CTAs per row, 16-byte units only
-    assert gtms.kernel_name(0, 16384, F32) == "gtms_fwd_cluster_kernel<f32,cluster2,team512,x4,minb0>"
-    assert gtms.kernel_name(1, 65536, BF16) == "gtms_bwd_cluster_kernel<bf16,cluster8,team128,x8,minb0>"
-    assert gtms.kernel_name(0, 8200, F16) == "gtms_fwd_cluster_kernel<f16,cluster2,team256,x4,minb0>"
+    assert gtms.kernel_name(0, 16384, F32) == "gtms_fwd_vec_kernel<f32,team1024,x4,minb0>"
+    assert gtms.kernel_name(0, 32768, F32) == "gtms_fwd_cluster_kernel<f32,cluster2,team1024,x4,minb0>"
+    assert gtms.kernel_name(0, 65536, F32) == "gtms_fwd_cluster_kernel<f32,cluster4,team1024,x4,minb0>"
+    assert gtms.kernel_name(1, 65536, BF16) == "gtms_bwd_cluster_kernel<bf16,cluster2,team512,x8,minb0>"
+    assert gtms.kernel_name(1, 32768, BF16) == "gtms_bwd_vec_kernel<bf16,team512,x8,minb0>"
+    assert gtms.kernel_name(0, 8200, F16) == "gtms_fwd_vec_kernel<f16,team512,x4,minb2>"
     assert gtms.kernel_name(0, 16384, F32, aligned16=False) == "none"
     # out of range
     assert gtms.kernel_name(0, 8193, F32) == "none"
@@ -131,6 +134,20 @@ def test_mask_arguments(lib):
         assert fn(*ptrs, 2, 3, 64, 1.0, 2, -4, F32, None) == INVALID
         assert fn(*ptrs, 0, 3, 64, 1.0, 2, 4, F32, None) == OK               # empty work
         assert fn(*ptrs, 2, 3, 64, float("nan"), 1, 0, F32, None) == INVALID
+
+
+def test_explicit_mask_arguments(lib):
+    MASK = 0x50_0000_0000
+    f, b = gtms.gtms_forward_explicit, gtms.gtms_backward_explicit
+    for fn, ptrs in ((f, (X, Y)), (b, (X, DY, Y))):
+        assert fn(*ptrs, None, 1, 2, 3, 64, 1.0, F32, None) == INVALID          # null mask
+        assert fn(*ptrs, MASK + 4, 1, 2, 3, 64, 1.0, F32, None) == INVALID      # mask not 8-byte aligned
+        assert fn(*ptrs, MASK, 3, 2, 3, 64, 1.0, F32, None) == INVALID          # mask_batches not 1 or B
+        assert fn(*ptrs, Y + 64, 2, 2, 3, 64, 1.0, F32, None) == INVALID        # mask inside the output
+        assert fn(*ptrs, MASK, 1, 2, 3, 63, 1.0, F32, None) == UNSUPPORTED      # rows not 16-byte multiples
+        assert fn(*ptrs, MASK, 1, 2, 3, 8200, 1.0, F32, None) == UNSUPPORTED    # longer than 8192
+        assert fn(*ptrs, MASK, 1, 0, 3, 64, 1.0, F32, None) == OK               # empty work
+        assert fn(*ptrs, MASK, 1, 2, 3, 64, 1.0, 5, None) == UNSUPPORTED        # unknown dtype
 
 
 @pytest.mark.parametrize("call", [fwd, bwd])

@@ -358,10 +358,11 @@ def test_long_rows_full_comparison(dev, S, dtype):
 
 
 @pytest.mark.parametrize("S,dtype,L", [(32768, "f32", 20001), (32768, "bf16", 32768), (65536, "bf16", 40000),
-                                       (65536, "f16", 65536)])
+                                       (65536, "f16", 65536), (65536, "f32", 30001)])
 def test_long_rows_sampled(dev, S, dtype, L):
-    """Largest rows: sampled rows element by element, every row's masked bits and
-    live row sums on the device."""
+    """Largest rows (one 1024-thread CTA up to 64 KB, a cluster of 2 or 4 CTAs
+    beyond): sampled rows element by element, every row's masked bits and live
+    row sums on the device."""
     w = si.custom(f"long{S}", 1, 1, S, dtype, 0.125, seq_lens=(L,), seed=S + L)
     lens = si.seq_lens(w)
     lens_d = torch.from_numpy(lens).to(dev)
@@ -473,3 +474,83 @@ def test_wide_window_equals_default_op(dev):
     d2 = gtms.backward(y0, dy, lens_d, mask_kind=2, window=5000)
     torch.cuda.synchronize()
     assert torch.equal(y0, y2) and torch.equal(d0, d2)
+
+
+# ---------------------------------------------------------------------------
+# Explicit keep mask ("优化ScaledMaskSoftmax算子" sections 2.2 / 3.1 / 4.1)
+# ---------------------------------------------------------------------------
+
+def _random_keep_mask(mb, S, seed, density=0.3):
+    g = torch.Generator().manual_seed(seed)
+    m = (torch.rand(mb, S, S, generator=g) < density).to(torch.uint8)
+    m[:, 1, :] = 0                 # an all-masked row
+    m[:, 2, :] = 1                 # a fully kept row
+    m[:, 3, :] = 0
+    m[:, 3, S - 1] = 1             # one kept entry, in the row's last unit
+    return m
+
+
+@pytest.mark.parametrize("S,dtype,mb", [(64, "f32", 1), (1000, "f32", 2), (2048, "bf16", 1), (2048, "f16", 2),
+                                        (8192, "f16", 1), (8192, "f32", 2), (24, "bf16", 2)])
+def test_explicit_mask_matches_oracle(dev, S, dtype, mb):
+    B, M = 2, 2 if S <= 2048 else 1
+    w = si.custom("explicit", B, M, S, dtype, 0.125 if dtype != "f32" else 1.0, seq_lens=(S,) * B, x_std=2.0,
+                  seed=S + mb)
+    mask = _random_keep_mask(mb, S, seed=S * 3 + mb)
+    mask_d = mask.to(dev)
+    x = si.make_x(w, "cpu")
+    dy = si.make_dy(w, "cpu")
+    y = gtms.forward_explicit(x.to(dev), mask_d, w.scale)
+    torch.cuda.synchronize()
+    xb, yb = to_bits(x, dtype).reshape(-1), to_bits(y, dtype).reshape(-1)
+    keep = mask.numpy().astype(bool)
+    code = w.dtype_code
+    ref = oracle.forward_explicit(xb, mask.numpy(), B, M, S, w.scale, code, threads=8)
+    st = Stats()
+    q = np.arange(B * M * S)
+    kept_rows = keep[(q // (M * S)) if mb == B else np.zeros_like(q), q % S]          # [rows, S]
+    _compare_explicit(yb.reshape(-1, S), ref, kept_rows, dtype, st)
+    assert st.ok, f"explicit forward {w.describe()}: {st}"
+    y_or = oracle.round_to(ref, code)
+    dx = gtms.backward_explicit(from_bits(y_or, dtype, "cpu").view(x.shape).to(dev), dy.to(dev), mask_d, w.scale)
+    torch.cuda.synchronize()
+    refb = oracle.backward_explicit(y_or, to_bits(dy, dtype).reshape(-1), mask.numpy(), B, M, S, w.scale, code,
+                                    threads=8)
+    sb = Stats()
+    _compare_explicit(to_bits(dx, dtype).reshape(-1, S), refb, kept_rows, dtype, sb)
+    assert sb.ok, f"explicit backward {w.describe()}: {sb}"
+
+
+def _compare_explicit(gpu_bits, ref, kept_rows, dtype, stats):
+    """compare_rows with an arbitrary kept set: masked bits must be zero, kept values within tolerance."""
+    from parity_utils import compare_rows
+
+    S = gpu_bits.shape[1]
+    # kept entries are compared through compare_rows one row at a time via their (c0, c1) = (0, S) and a
+    # zeroed reference where masked; masked bits are checked separately
+    stats.bad_masked += int(np.count_nonzero(gpu_bits[~kept_rows]))
+    g = np.where(kept_rows, gpu_bits, 0).astype(gpu_bits.dtype)
+    full = (np.zeros(len(g), np.int64), np.full(len(g), S, np.int64))
+    compare_rows(g, np.where(kept_rows, ref, 0.0), full, dtype, stats)
+
+
+def test_explicit_mask_inputs_not_read_and_tril_equivalence(dev):
+    S, B, M = 1000, 2, 2
+    w = si.custom("explicit_tril", B, M, S, "f32", 1.0, seq_lens=(S, 600), seed=77)
+    lens = si.seq_lens(w)
+    r, c = torch.arange(S)[:, None], torch.arange(S)[None, :]
+    tril = torch.stack([((c <= r) & (r < int(L))) for L in lens]).to(torch.uint8).to(dev)
+    x = si.make_x(w, dev)
+    dy = si.make_dy(w, dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    y_ref = gtms.forward(x, lens_d)
+    y = gtms.forward_explicit(x, tril)
+    x_nan = torch.where(tril[:, None].bool(), x, float("nan"))
+    y_nan = gtms.forward_explicit(x_nan, tril)
+    d_ref = gtms.backward(y_ref, dy, lens_d)
+    d = gtms.backward_explicit(y_ref, torch.where(tril[:, None].bool(), dy, float("nan")), tril)
+    torch.cuda.synchronize()
+    # same kept set and same arithmetic as the grouped-tril kernel, up to reduction order
+    assert torch.equal(y_nan, y)
+    assert float((y - y_ref).abs().max()) <= 2e-6 and float((d - d_ref).abs().max()) <= 2e-6
+    assert masked_bits_all_zero(y, lens_d, "f32") and masked_bits_all_zero(d, lens_d, "f32")
