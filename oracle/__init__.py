@@ -69,6 +69,8 @@ def _load():
             lib.gtms_oracle_backward_explicit.argtypes = [vp, vp, ci, vp, i64, i64, i64, i64, dp, i64, i64, vp]
             lib.gtms_oracle_forward_explicit.restype = ctypes.c_int
             lib.gtms_oracle_backward_explicit.restype = ctypes.c_int
+            lib.gtms_oracle_attn_dscores.argtypes = [vp, vp, vp, ci, vp, i64, i64, i64, i64, dp, i64, i64, vp]
+            lib.gtms_oracle_attn_dscores.restype = ctypes.c_int
             lib.gtms_oracle_round.argtypes = [vp, i64, ctypes.c_int, vp]
             lib.gtms_oracle_decode.argtypes = [vp, i64, ctypes.c_int, vp]
             for f in (lib.gtms_oracle_forward, lib.gtms_oracle_backward,
@@ -191,6 +193,40 @@ def backward_explicit(y, dy, mask, B, M, S, scale, dtype, row_begin=0, row_end=N
     row_end = B * M * S if row_end is None else row_end
     return _run_explicit("gtms_oracle_backward_explicit", [y, dy], dtype, mask, B, M, S, scale, row_begin, row_end,
                          threads)
+
+
+def attn_dscores(p, dout, v, seq_lens, B, M, S, d, scale, dtype, row_begin=0, row_end=None, threads=1):
+    """Attention-backward step dS = scale * P * (dP - rowsum(dP * P)), dP = dO V^T, grouped tril mask
+    ("ops(8): self-attention 的 CUDA 实现及优化 (下)", section 2.1). ``p`` holds rows [row_begin, row_end)
+    of P [B,M,S,S]; ``dout`` and ``v`` are whole [B,M,S,d] tensors. Float64 [rows, S]."""
+    lib = _load()
+    row_end = B * M * S if row_end is None else row_end
+    seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    pa = _as_bits(np.asarray(p), dtype).reshape(-1)
+    da = _as_bits(np.asarray(dout), dtype).reshape(-1)
+    va = _as_bits(np.asarray(v), dtype).reshape(-1)
+    rows = row_end - row_begin
+    if seq.shape != (B,) or pa.size != rows * S or da.size != B * M * S * d or va.size != B * M * S * d:
+        raise ValueError("attn_dscores: shapes do not match")
+    out = np.empty((rows, S), dtype=np.float64)
+    eb = _ELEM_BYTES[dtype]
+
+    def work(chunk):
+        r0, r1 = chunk
+        off = (r0 - row_begin) * S
+        rc = lib.gtms_oracle_attn_dscores(ctypes.c_void_p(pa.ctypes.data + off * eb), da.ctypes.data, va.ctypes.data,
+                                          dtype, seq.ctypes.data, B, M, S, d, float(scale), r0, r1,
+                                          ctypes.c_void_p(out.ctypes.data + off * 8))
+        if rc != 0:
+            raise ValueError("gtms_oracle_attn_dscores rejected its arguments")
+
+    chunks = _row_chunks(row_begin, row_end, threads)
+    if len(chunks) == 1:
+        work(chunks[0])
+    else:
+        with _cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(work, chunks))
+    return out
 
 
 def round_to(values, dtype: int) -> np.ndarray:

@@ -54,6 +54,13 @@
  * uint8 [mask_batches, S, S] with mask_batches 1 (one mask for every batch) or
  * B, and is shared by the M heads.
  *
+ * Attention-backward step ("ops(8): self-attention 的 CUDA 实现及优化 (下)", section
+ * 2.1: with P = softmax(S), O = P V the backward runs dP = dO V^T, then
+ * dS = softmax-backward(dP, P)). gtms_oracle_attn_dscores forms, for each row,
+ * dP_rc = sum_k dO_rk V_ck on the kept columns (grouped tril mask) and
+ * dS_rc = scale * P_rc * (dP_rc - sum_c' dP_rc' P_rc'), +0.0 elsewhere; dO and
+ * V are [B, M, S, d].
+ *
  * Build: cc -O2 -fno-fast-math -fPIC -shared gtms_oracle.c -o libgtms_oracle.so -lm
  */
 #include <math.h>
@@ -307,6 +314,40 @@ int gtms_oracle_backward(const void* y, const void* dy, int dtype, const int32_t
                          int64_t row_begin, int64_t row_end, double* dx)
 {
     return gtms_oracle_backward_masked(y, dy, dtype, seq_lens, B, M, S, scale, 0, 0, row_begin, row_end, dx);
+}
+
+/* ---- attention-backward step: dS from P, dO, V ----
+ * p: rows [row_begin, row_end) of P[B,M,S,S]; dout, v: the whole [B,M,S,d]
+ * tensors. ds: (row_end - row_begin) * S doubles. */
+int gtms_oracle_attn_dscores(const void* p, const void* dout, const void* v, int dtype, const int32_t* seq_lens,
+                             int64_t B, int64_t M, int64_t S, int64_t d, double scale,
+                             int64_t row_begin, int64_t row_end, double* ds)
+{
+    if (dtype < ORC_F32 || dtype > ORC_F64 || bad_shape(B, M, S, row_begin, row_end) || d < 1)
+        return ORC_BAD_ARG;
+    for (int64_t q = row_begin; q < row_end; ++q) {
+        const int64_t base = (q - row_begin) * S;
+        int64_t c0, c1;
+        kept_range(seq_lens, M, S, 0, 0, q, &c0, &c1);
+        const int64_t slice = q / S;               /* (b, m) */
+        const int64_t r = q % S;
+        double* dsr = ds + base;
+        for (int64_t c = 0; c < S; ++c)
+            dsr[c] = 0.0;
+        if (c1 <= c0)
+            continue;
+        double dot = 0.0;                          /* sum_c dP_rc P_rc */
+        for (int64_t c = c0; c < c1; ++c) {
+            double dp = 0.0;
+            for (int64_t k = 0; k < d; ++k)
+                dp += load_elem(dout, (slice * S + r) * d + k, dtype) * load_elem(v, (slice * S + c) * d + k, dtype);
+            dsr[c] = dp;                           /* dP held here until the second loop */
+            dot += dp * load_elem(p, base + c, dtype);
+        }
+        for (int64_t c = c0; c < c1; ++c)
+            dsr[c] = scale * load_elem(p, base + c, dtype) * (dsr[c] - dot);
+    }
+    return ORC_OK;
 }
 
 /* ---- explicit mask ---- */

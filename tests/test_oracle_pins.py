@@ -548,3 +548,38 @@ def test_explicit_mask_backward_matches_central_differences():
                                - (_fwd64_explicit(xm, keep, scale) * dy).sum()) / (2 * h)
     np.testing.assert_allclose(dx, num, rtol=0, atol=1e-8)
     assert np.all(dx[0, 0][keep[0] == 0] == 0.0)
+
+
+# ---------------------------------------------------------------------------
+# Attention-backward step ("ops(8)" section 2.1): dS from P, dO, V
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S,d,L", [(8, 4, 8), (17, 16, 11), (33, 8, 0)])
+def test_attn_dscores_matches_autograd_through_pv(S, d, L):
+    """X.grad of O = masked_softmax(scale * X) V under upstream dO is the fused step's dS."""
+    g = torch.Generator().manual_seed(500 + S + d + L)
+    B, M, scale = 2, 2, 0.35
+    x = (torch.randn(B, M, S, S, generator=g, dtype=torch.float64) * 2).requires_grad_(True)
+    v = torch.randn(B, M, S, d, generator=g, dtype=torch.float64)
+    dout = torch.randn(B, M, S, d, generator=g, dtype=torch.float64)
+    causal = torch.triu(torch.ones(S, S, dtype=torch.bool), 1)
+    keep = torch.zeros(S, S, dtype=torch.float64)
+    keep[:L] = 1.0
+    p = torch.softmax((x * scale).masked_fill(causal, float("-inf")), dim=-1) * keep
+    (p @ v).backward(dout)
+    sl = np.array([L, L], np.int32)
+    ds = oracle.attn_dscores(p.detach().numpy(), dout.numpy(), v.numpy(), sl, B, M, S, d, scale, F64)
+    np.testing.assert_allclose(ds.reshape(B, M, S, S), x.grad.numpy(), rtol=0, atol=1e-13)
+
+
+def test_attn_dscores_is_softmax_backward_of_dp():
+    rng = np.random.default_rng(24)
+    B, M, S, d = 2, 1, 12, 5
+    x = rng.standard_normal((B, M, S, S))
+    v = rng.standard_normal((B, M, S, d))
+    dout = rng.standard_normal((B, M, S, d))
+    sl = np.array([12, 7], np.int32)
+    p = _fwd64(x, sl, 0.5)
+    dp = dout @ np.swapaxes(v, -1, -2)
+    ds = oracle.attn_dscores(p, dout, v, sl, B, M, S, d, 0.5, F64, threads=3).reshape(B, M, S, S)
+    np.testing.assert_allclose(ds, _bwd64(p, dp, sl, 0.5), rtol=0, atol=1e-13)
