@@ -160,6 +160,32 @@ int gtms_forward_explicit(const void* x, void* y, const uint8_t* mask, int64_t m
 int gtms_backward_explicit(const void* y, const void* dy, void* dx, const uint8_t* mask, int64_t mask_batches,
                            int64_t B, int64_t M, int64_t S, float scale, int dtype, void* stream);
 
+/*
+ * Attention-backward step around the masked softmax, fused with its GEMM on the
+ * tensor cores ("ops(8): self-attention 的 CUDA 实现及优化 (下)", section 2.1: with
+ * P the softmax output, O = P V and upstream gradient dO, the backward forms
+ * dP = dO V^T and then the softmax backward of dP):
+ *   dS[b,m,r,c] = scale * P[b,m,r,c] * (dP[r,c] - sum_c' dP[r,c'] P[b,m,r,c'])
+ * on the grouped-tril kept entries (c <= r < L), +0.0 elsewhere, with
+ * dP[r,c] = sum_k dO[b,m,r,k] V[b,m,c,k] accumulated in fp32 and never
+ * written to memory.
+ *   p        device, [B,M,S,S] of `dtype` (the forward output), read-only;
+ *            only 16-byte units holding a kept entry are loaded.
+ *   dout, v  device, [B,M,S,head_dim] of `dtype`, read-only.
+ *   ds       device, [B,M,S,S] of `dtype`, every element written; may equal p.
+ *   seq_lens device int32[B]; scale finite.
+ *   head_dim 64 or 128; dtype GTMS_BF16 or GTMS_F16; S a multiple of 8.
+ *   status   NULL, or a device int32 the kernel ORs 1 into if one of its
+ *            bounded internal waits ran out (the caller clears it); results
+ *            are then incomplete.
+ * All pointers 16-byte aligned (status 4-byte). GTMS_ERR_UNSUPPORTED: fp32,
+ * other head dims, S not a multiple of 8, S > GTMS_MAX_S. Otherwise as
+ * gtms_backward.
+ */
+int gtms_attention_softmax_backward(const void* p, const void* dout, const void* v, void* ds, const int32_t* seq_lens,
+                                    int64_t B, int64_t M, int64_t S, int64_t head_dim, float scale, int dtype,
+                                    int32_t* status, void* stream);
+
 /* Static, NUL-terminated name of a status code ("GTMS_OK", ...). */
 const char* gtms_status_string(int status);
 

@@ -28,7 +28,8 @@ GTMS_MASK_GROUPED_TRIL, GTMS_MASK_LENGTH, GTMS_MASK_SLIDING_WINDOW = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gtms_forward", "gtms_backward", "gtms_status_string", "gtms_version",
                     "gtms_kernel_name", "gtms_device_pointer_of_host", "gtms_forward_masked",
-                    "gtms_backward_masked", "gtms_forward_explicit", "gtms_backward_explicit")
+                    "gtms_backward_masked", "gtms_forward_explicit", "gtms_backward_explicit",
+                    "gtms_attention_softmax_backward")
 
 _lib = None
 _lock = threading.Lock()
@@ -69,6 +70,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.gtms_forward_explicit.restype = ctypes.c_int
         lib.gtms_backward_explicit.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
         lib.gtms_backward_explicit.restype = ctypes.c_int
+        lib.gtms_attention_softmax_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float,
+                                                        ctypes.c_int, vp, vp]
+        lib.gtms_attention_softmax_backward.restype = ctypes.c_int
         lib.gtms_status_string.argtypes = [ctypes.c_int]
         lib.gtms_status_string.restype = ctypes.c_char_p
         lib.gtms_version.argtypes = []
@@ -108,6 +112,12 @@ def gtms_forward_explicit(x, y, mask, mask_batches, B, M, S, scale, dtype, strea
 
 def gtms_backward_explicit(y, dy, dx, mask, mask_batches, B, M, S, scale, dtype, stream) -> int:
     return load_library().gtms_backward_explicit(y, dy, dx, mask, mask_batches, B, M, S, scale, dtype, stream)
+
+
+def gtms_attention_softmax_backward(p, dout, v, ds, seq_lens, B, M, S, head_dim, scale, dtype, status,
+                                    stream) -> int:
+    return load_library().gtms_attention_softmax_backward(p, dout, v, ds, seq_lens, B, M, S, head_dim, scale, dtype,
+                                                          status, stream)
 
 
 def status_string(status: int) -> str:
@@ -247,6 +257,33 @@ def backward_explicit(y, dy, mask, scale: float = 1.0, out=None):
     if rc != GTMS_OK:
         raise GtmsError("gtms_backward_explicit", rc)
     return dx
+
+
+def attention_softmax_backward(p, dout, v, seq_lens, scale: float = 1.0, out=None, status=None):
+    """dS = scale * P * (dO V^T - rowsum(dO V^T * P)) on the grouped-tril kept entries, with the GEMM on the
+    tensor cores; ``p`` [B,M,S,S], ``dout`` / ``v`` [B,M,S,d] (d 64 or 128), bf16 or fp16. ``status`` (an
+    optional int32 CUDA tensor of one element) receives 1 if an internal wait of the kernel ran out."""
+    import torch
+
+    _check_scores("p", p)
+    B, M, S, _ = p.shape
+    for name, t in (("dout", dout), ("v", v)):
+        if t.dim() != 4 or t.shape[:3] != p.shape[:3] or t.dtype != p.dtype or t.device != p.device \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, M, S, d] tensor matching p")
+    if dout.shape != v.shape:
+        raise ValueError("dout and v must have the same shape")
+    _check_lens(seq_lens, B, p.device)
+    ds = torch.empty_like(p) if out is None else out
+    if ds.shape != p.shape or ds.dtype != p.dtype or ds.device != p.device or not ds.is_contiguous():
+        raise ValueError("out must match p in shape, dtype, device and be contiguous")
+    stream = torch.cuda.current_stream(p.device).cuda_stream
+    rc = gtms_attention_softmax_backward(p.data_ptr(), dout.data_ptr(), v.data_ptr(), ds.data_ptr(),
+                                         seq_lens.data_ptr(), B, M, S, dout.shape[3], float(scale), _dtype_code(p),
+                                         None if status is None else status.data_ptr(), stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_attention_softmax_backward", rc)
+    return ds
 
 
 def _check_pinned(name, t):

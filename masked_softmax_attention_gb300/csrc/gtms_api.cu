@@ -48,6 +48,21 @@ GTMS_EXTERN_EXPLICIT(float)
 GTMS_EXTERN_EXPLICIT(__nv_bfloat16)
 GTMS_EXTERN_EXPLICIT(__half)
 #undef GTMS_EXTERN_EXPLICIT
+template <typename T, int D>
+cudaError_t launch_attn_dscores(const void*, const void*, const void*, void*, const int32_t*, int64_t, int64_t,
+                                int64_t, float, int32_t*, cudaStream_t);
+extern template cudaError_t launch_attn_dscores<__nv_bfloat16, 64>(const void*, const void*, const void*, void*,
+                                                                   const int32_t*, int64_t, int64_t, int64_t, float,
+                                                                   int32_t*, cudaStream_t);
+extern template cudaError_t launch_attn_dscores<__nv_bfloat16, 128>(const void*, const void*, const void*, void*,
+                                                                    const int32_t*, int64_t, int64_t, int64_t, float,
+                                                                    int32_t*, cudaStream_t);
+extern template cudaError_t launch_attn_dscores<__half, 64>(const void*, const void*, const void*, void*,
+                                                            const int32_t*, int64_t, int64_t, int64_t, float,
+                                                            int32_t*, cudaStream_t);
+extern template cudaError_t launch_attn_dscores<__half, 128>(const void*, const void*, const void*, void*,
+                                                             const int32_t*, int64_t, int64_t, int64_t, float,
+                                                             int32_t*, cudaStream_t);
 }  // namespace gtms
 
 namespace {
@@ -303,6 +318,47 @@ GTMS_EXPORT int gtms_backward_explicit(const void* y, const void* dy, void* dx, 
     default: gtms::launch_backward_explicit<__half>(variant, y, dy, dx, mask, mb, g, scale, st); break;
     }
     return launch_status();
+}
+
+GTMS_EXPORT int gtms_attention_softmax_backward(const void* p, const void* dout, const void* v, void* ds,
+                                                const int32_t* seq_lens, int64_t B, int64_t M, int64_t S,
+                                                int64_t head_dim, float scale, int dtype, int32_t* status,
+                                                void* stream)
+{
+    const Checked c = check_shape(B, M, S, scale, dtype);
+    if (c.status != GTMS_OK)
+        return c.status;
+    if (head_dim < 0)
+        return GTMS_ERR_INVALID_ARG;
+    if (dtype == GTMS_F32 || (head_dim != 64 && head_dim != 128) || S % 8 != 0)
+        return GTMS_ERR_UNSUPPORTED;
+    if (c.rows == 0)
+        return GTMS_OK;
+    const int64_t nrb = (S + 127) / 128;
+    if (B * M > INT32_MAX / nrb)
+        return GTMS_ERR_UNSUPPORTED;
+    if (!p || !dout || !v || !ds || !seq_lens)
+        return GTMS_ERR_INVALID_ARG;
+    if (!aligned_to(p, 16) || !aligned_to(dout, 16) || !aligned_to(v, 16) || !aligned_to(ds, 16) ||
+        !aligned_to(seq_lens, 4) || (status && !aligned_to(status, 4)))
+        return GTMS_ERR_INVALID_ARG;
+    const uint64_t ob = static_cast<uint64_t>(B) * M * S * head_dim * 2;   // dO and V bytes
+    if (bad_alias(ds, p, c.bytes) || overlaps(ds, c.bytes, dout, ob) || overlaps(ds, c.bytes, v, ob) ||
+        overlaps(ds, c.bytes, seq_lens, static_cast<uint64_t>(B) * 4) || (status && overlaps(ds, c.bytes, status, 4)))
+        return GTMS_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dtype == GTMS_BF16)
+        e = head_dim == 64 ? gtms::launch_attn_dscores<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
+                           : gtms::launch_attn_dscores<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+    else
+        e = head_dim == 64 ? gtms::launch_attn_dscores<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
+                           : gtms::launch_attn_dscores<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GTMS_ERR_CUDA;
+    }
+    return GTMS_OK;
 }
 
 GTMS_EXPORT int gtms_device_pointer_of_host(const void* host, void** device)

@@ -136,6 +136,30 @@ def test_mask_arguments(lib):
         assert fn(*ptrs, 2, 3, 64, float("nan"), 1, 0, F32, None) == INVALID
 
 
+def test_attention_softmax_backward_arguments(lib):
+    fn = gtms.gtms_attention_softmax_backward
+    DO, V, DS, ST = 0x60_0000_0000, 0x70_0000_0000, 0x80_0000_0000, 0x90_0000_0000
+    args = dict(B=2, M=3, S=256, d=64, scale=0.125, dtype=BF16)
+
+    def call(p=X, dout=DO, v=V, ds=DS, lens=LENS, status=ST, **kw):
+        a = {**args, **kw}
+        return fn(p, dout, v, ds, lens, a["B"], a["M"], a["S"], a["d"], a["scale"], a["dtype"], status, None)
+
+    assert call(dtype=F32) == UNSUPPORTED          # tensor-core path is 16-bit only
+    assert call(d=96) == UNSUPPORTED                # head dims 64 and 128
+    assert call(S=260) == UNSUPPORTED               # S multiple of 8
+    assert call(S=gtms.GTMS_MAX_S + 8) == UNSUPPORTED
+    assert call(d=-64) == INVALID
+    assert call(p=None) == INVALID and call(v=None) == INVALID and call(lens=None) == INVALID
+    assert call(dout=DO + 8) == INVALID             # 16-byte alignment
+    assert call(status=ST + 2) == INVALID
+    assert call(ds=X + 32) == INVALID               # partial overlap with p
+    assert call(ds=DO + 64) == INVALID              # overlap with dO
+    assert call(status=DS + 4) == INVALID           # status inside the output
+    assert call(B=0, p=None, dout=None, v=None, ds=None, lens=None) == OK
+    assert call(scale=float("inf")) == INVALID
+
+
 def test_explicit_mask_arguments(lib):
     MASK = 0x50_0000_0000
     f, b = gtms.gtms_forward_explicit, gtms.gtms_backward_explicit

@@ -554,3 +554,82 @@ def test_explicit_mask_inputs_not_read_and_tril_equivalence(dev):
     assert torch.equal(y_nan, y)
     assert float((y - y_ref).abs().max()) <= 2e-6 and float((d - d_ref).abs().max()) <= 2e-6
     assert masked_bits_all_zero(y, lens_d, "f32") and masked_bits_all_zero(d, lens_d, "f32")
+
+
+# ---------------------------------------------------------------------------
+# Attention-backward step fused with its tensor-core GEMM ("ops(8)" section 2.1)
+# ---------------------------------------------------------------------------
+
+def _attn_case(dev, B, M, S, d, dtype, lens, seed, scale=0.125):
+    """P = the oracle's forward of seeded scores (rounded to the IO dtype), dO, V ~ N(0,1)."""
+    w = si.custom("attn", B, M, S, dtype, scale, seq_lens=lens, x_std=2.0, seed=seed)
+    x_bits = to_bits(si.make_x(w, "cpu"), dtype)
+    p_bits = oracle_forward_bits(x_bits, si.seq_lens(w), B, M, S, scale, dtype)
+    g = torch.Generator().manual_seed(seed + 1)
+    tdt = si.TORCH_DTYPES[dtype]
+    dout = torch.randn(B, M, S, d, generator=g).to(tdt)
+    v = torch.randn(B, M, S, d, generator=g).to(tdt)
+    return w, p_bits, dout, v
+
+
+def _attn_check(w, d, p_bits, dout, v, ds_dev, tag):
+    """Element-wise: masked entries +0.0 bits; kept entries within
+    ulp(ref) + scale * P * d * 2^-23 * (A_rc + max_c' A_rc'), A = |dO| |V|^T:
+    the bound of an fp32 accumulation of the d exact products of dP, and of its
+    propagation through the row sum (P sums to 1)."""
+    B, M, S, dt = w.B, w.M, w.S, w.dtype
+    lens = si.seq_lens(w)
+    code = w.dtype_code
+    db, vb = to_bits(dout, dt), to_bits(v, dt)
+    ref = oracle.attn_dscores(p_bits, db, vb, lens, B, M, S, d, w.scale, code, threads=8).reshape(B, M, S, S)
+    got = to_bits(ds_dev, dt).reshape(B, M, S, S)
+    pv = oracle.decode(p_bits, code).reshape(B, M, S, S)
+    A = np.abs(oracle.decode(db, code)) @ np.swapaxes(np.abs(oracle.decode(vb, code)), -1, -2)   # [B,M,S,S]
+    c0, c1 = oracle.kept_ranges(lens, S)
+    col = np.arange(S)[None, None, None, :]
+    kept = (col >= c0[:, None, :, None]) & (col < c1[:, None, :, None])
+    kept = np.broadcast_to(kept, ref.shape)
+    assert np.count_nonzero(got[~kept]) == 0, f"{tag}: masked output not +0.0"
+    Amax = np.where(kept, A, 0.0).max(axis=-1, keepdims=True)
+    # one ulp of the IO dtype at |ref|: the gap to the next representable magnitude
+    rb = oracle.round_to(np.abs(ref), code).astype(np.int64)
+    top = 0x7BFF if dt == "f16" else 0x7F7F
+    nb = np.where(rb < top, rb + 1, rb - 1)
+    ulp = np.abs(oracle.decode(nb.astype(np.uint16), code) - oracle.decode(rb.astype(np.uint16), code))
+    tol = ulp + abs(w.scale) * pv * d * 2.0 ** -23 * (A + Amax)
+    err = np.abs(oracle.decode(got, code) - ref)
+    bad = kept & (err > tol)
+    assert not bad.any(), f"{tag}: {int(bad.sum())} of {int(kept.sum())} kept entries out of tolerance, " \
+                          f"worst excess {float((err - tol)[kept].max()):.3g}"
+
+
+@pytest.mark.parametrize("S,d,dtype,lens", [(8, 64, "bf16", (8, 3)), (128, 64, "bf16", (128, 77)),
+                                             (200, 128, "f16", (200, 0)), (1000, 64, "bf16", (1000, 513)),
+                                             (1024, 128, "bf16", (700, 1024)), (2048, 64, "f16", (2048, 1300))])
+def test_attention_softmax_backward_matches_oracle(dev, S, d, dtype, lens):
+    B, M = 2, 2 if S <= 1024 else 1
+    w, p_bits, dout, v = _attn_case(dev, B, M, S, d, dtype, lens, seed=S + d)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    p_d = from_bits(p_bits, dtype, "cpu").view(B, M, S, S).to(dev)
+    ds = torch.full_like(p_d, float("nan"))
+    gtms.attention_softmax_backward(p_d, dout.to(dev), v.to(dev), torch.from_numpy(si.seq_lens(w)).to(dev),
+                                    w.scale, out=ds, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _attn_check(w, d, p_bits, dout, v, ds, f"S={S} d={d} {dtype}")
+
+
+def test_attention_softmax_backward_in_place_and_masked_p_not_read(dev):
+    B, M, S, d, dtype = 2, 2, 384, 64, "bf16"
+    w, p_bits, dout, v = _attn_case(dev, B, M, S, d, dtype, (384, 200), seed=90)
+    lens_d = torch.from_numpy(si.seq_lens(w)).to(dev)
+    p_d = from_bits(p_bits, dtype, "cpu").view(B, M, S, S).to(dev)
+    ref = gtms.attention_softmax_backward(p_d, dout.to(dev), v.to(dev), lens_d, w.scale)
+    # NaN in every masked P entry must not reach dS; dS may overwrite P
+    kept = torch.from_numpy(oracle.kept_prefix_lengths(si.seq_lens(w), M, S)).to(dev)
+    col = torch.arange(S, device=dev)
+    keep = (col[None, None, :] < kept[:, :, None])[:, None]
+    p_nan = torch.where(keep, p_d, torch.tensor(float("nan"), dtype=p_d.dtype, device=dev))
+    got = gtms.attention_softmax_backward(p_nan, dout.to(dev), v.to(dev), lens_d, w.scale, out=p_nan)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
