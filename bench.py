@@ -179,25 +179,51 @@ def oracle_sample(w, lens, slices, device="cpu"):
     picked = [b for b, _ in slices]
     ws = si.Workload(w.name + "_sample", len(picked), 1, w.S, w.dtype, w.scale, x_std=w.x_std,
                      fixed_seq_lens=tuple(int(lens[b]) for b in picked), spike_prob=w.spike_prob,
-                     spike_value=w.spike_value, backward=w.backward, seed=w.seed + 7)
-    x = si.make_x(ws, device)
-    dy = si.make_dy(ws, device)
+                     spike_value=w.spike_value, backward=w.backward, seed=w.seed + 7, head_dim=w.head_dim)
     bits_t = {"f32": (np.uint32, "int32"), "bf16": (np.uint16, "int16"), "f16": (np.uint16, "int16")}[w.dtype]
     import torch
 
     tview = getattr(torch, bits_t[1])
-    xb = x.view(tview).numpy().view(bits_t[0])
-    dyb = dy.view(tview).numpy().view(bits_t[0])
-    return ws, xb, dyb
+
+    def bits(t):
+        return t.view(tview).numpy().view(bits_t[0])
+
+    xb = bits(si.make_x(ws, device))
+    if ws.head_dim > 0:
+        # attention-backward sample: P is the oracle's own (rounded) softmax of x; dO and V as drawn
+        import oracle
+
+        lens_s = np.array(ws.fixed_seq_lens, dtype=np.int32)
+        pb = oracle.round_to(oracle.forward(xb, lens_s, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code,
+                                            threads=os.cpu_count() or 1), ws.dtype_code)
+        dout, v = si.make_head_operands(ws, device)
+        return ws, pb, (bits(dout), bits(v))
+    return ws, xb, bits(si.make_dy(ws, device))
+
+
+def step_bytes(w, lens):
+    """Algorithmic bytes of one step: the softmax forward + backward, or for an
+    attention-backward workload the kept P read, every dS written, dO and V read."""
+    fb, bb = required_bytes(w, lens)
+    if w.head_dim > 0:
+        return fb + 2 * w.B * w.M * w.S * w.head_dim * w.elem_bytes
+    return fb + bb
 
 
 def oracle_step(ws, xb, dyb, threads):
-    """One oracle pass over the sample: forward, round, backward (all rows)."""
+    """One oracle pass over the sample: forward, round, backward (all rows); for an
+    attention-backward sample, the dS step from (P, dO, V) and its rounding."""
     import numpy as np
 
     import oracle
 
     lens = np.array(ws.fixed_seq_lens, dtype=np.int32)
+    if ws.head_dim > 0:
+        dout, v = dyb
+        ds = oracle.attn_dscores(xb, dout, v, lens, ws.B, ws.M, ws.S, ws.head_dim, ws.scale, ws.dtype_code,
+                                 threads=threads)
+        oracle.round_to(ds, ws.dtype_code)
+        return
     y = oracle.forward(xb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
     yb = oracle.round_to(y, ws.dtype_code)
     if ws.backward:
@@ -217,14 +243,17 @@ def cpu_baseline(w, lens, budget_s=12.0):
         t0 = time.perf_counter()
         oracle_step(ws, xb, dyb, threads)
         total_s += time.perf_counter() - t0
-        fb, bb = required_bytes(ws, ws.fixed_seq_lens)
-        total_bytes += fb + bb
+        total_bytes += step_bytes(ws, ws.fixed_seq_lens)
         done_slices += group
         groups += 1
     return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{done_slices} (b,m) slices of {w.name} (S={w.S}, the workload's seq_lens and value "
-                      f"distribution, drawn on the CPU) in {groups} groups: oracle forward + round + backward, "
+                      f"distribution, drawn on the CPU) in {groups} groups: {oracle_step_name(w)}, "
                       f"{total_s:.2f} s wall on {threads} threads"}
+
+
+def oracle_step_name(w):
+    return "oracle dS step from (P, dO, V) + round" if w.head_dim > 0 else "oracle forward + round + backward"
 
 
 def run_reference(args, w, lens):
@@ -239,10 +268,9 @@ def run_reference(args, w, lens):
     for _ in range(args.steps):
         oracle_step(ws, xb, dyb, threads)
     dt = (time.perf_counter() - t0) / max(1, args.steps)
-    fb, bb = required_bytes(ws, ws.fixed_seq_lens)
-    value = (fb + bb) / dt / 1e9
+    value = step_bytes(ws, ws.fixed_seq_lens) / dt / 1e9
     sample = (f"1 (b,m) slice of {w.name} per step (S={w.S}, seq_len={ws.fixed_seq_lens[0]}, drawn on the "
-              f"CPU): oracle forward + round + backward")
+              f"CPU): {oracle_step_name(w)}")
     line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
@@ -300,9 +328,141 @@ def workload_config(w, lens):
     fb, bb = required_bytes(w, lens)
     return {"workload": w.name + ": " + w.describe(), "B": w.B, "M": w.M, "S": w.S, "dtype": w.dtype,
             "scale": w.scale, "seq_lens_seeded": [int(v) for v in lens] if len(lens) <= 16 else "see seed",
-            "seed": w.seed, "required_bytes_fwd": fb, "required_bytes_bwd": bb,
-            "l2": "no flush: x, y, dy, dx are each larger than the 129 MB L2",
+            "seed": w.seed, **({"head_dim": w.head_dim, "required_bytes_step": step_bytes(w, lens)}
+                               if w.head_dim > 0 else {"required_bytes_fwd": fb, "required_bytes_bwd": bb}),
+            "l2": "no flush: " + ("P and dS are" if w.head_dim > 0 else "x, y, dy, dx are each")
+                  + " larger than the 129 MB L2",
             "parallelism": "one replica per GPU (rows independent, no collective)"}
+
+
+def run_gpu_attention(args, w, lens, rank, world, local_rank):
+    """The attention-backward step dS = scale * P * (dO V^T - rowsum(dO V^T * P)) (one fused launch).
+    Algorithmic bytes per (b, m) slice: kept P read once, every dS written, dO and V read once."""
+    import torch
+
+    import masked_softmax_attention_gb300 as gtms
+    import seeded_inputs as si
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    wr = replica_workload(w, rank)
+    lens_r = si.seq_lens(wr)
+    lens_d = torch.from_numpy(lens_r).to(dev)
+    p = gtms.forward(si.make_x(wr, dev), lens_d, wr.scale)
+    dout, v = si.make_head_operands(wr, dev)
+    ds = torch.empty_like(p)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fn = gtms.load_library().gtms_attention_softmax_backward
+    args_c = (p.data_ptr(), dout.data_ptr(), v.data_ptr(), ds.data_ptr(), lens_d.data_ptr(), wr.B, wr.M, wr.S,
+              wr.head_dim, float(wr.scale), wr.dtype_code, status.data_ptr(), stream.cuda_stream)
+    for _ in range(args.warmup):
+        if fn(*args_c):
+            raise RuntimeError("gtms_attention_softmax_backward failed")
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    s_ev.record(stream)
+    rc = 0
+    for _ in range(args.steps):
+        rc |= fn(*args_c)
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if rc or int(status.item()):
+        raise RuntimeError("gtms_attention_softmax_backward failed or timed out inside the timed region")
+    ms = max_over_ranks(s_ev.elapsed_time(e_ev) / args.steps, dist, dev)
+    fb, _ = required_bytes(wr, lens_r)                    # kept P read + every dS written
+    nbytes = fb + 2 * wr.B * wr.M * wr.S * wr.head_dim * wr.elem_bytes
+    value = whole_job_gbs(sum_over_ranks(nbytes, dist, dev), ms)
+    peak, peak_kind = hbm_peak()
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
+    e2e = None
+    if rank == 0 and args.e2e_steps > 0:
+        del ds
+        torch.cuda.empty_cache()
+        e2e = run_e2e_attention_host_resident(args, wr, lens_r, p, dout, v, stream, fn)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, lens)
+    if rank == 0:
+        kname = f"gtms_attn_dscores_kernel<{wr.dtype},d{wr.head_dim}>"
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        print(json.dumps({
+            "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {**workload_config(w, lens),
+                       "step": "gtms_attention_softmax_backward (dP = dO V^T on tcgen05, fused softmax backward)"},
+            "kernels": {"attention_softmax_backward": {"kernel": kname, "ms_per_call": round(ms, 5),
+                                                       "required_bytes": nbytes, "achieved_gbs": round(gbs, 2),
+                                                       "frac_of_peak": round(gbs / peak, 4)}},
+            "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'recipe fallback 6.8 TB/s'})",
+                         "algorithmic_bytes_per_launch": nbytes},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps, "clocks": clocks, "impl": "gtms"}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e_attention_host_resident(args, w, lens, p, dout, v, stream, fn):
+    """The attention-backward step through the C ABI with P, dO, V and dS in
+    pinned host memory, read and written by the kernel over the host link."""
+    import torch
+
+    import masked_softmax_attention_gb300 as gtms
+
+    try:
+        p_h = torch.empty(p.shape, dtype=p.dtype, pin_memory=True)
+        ds_h = torch.empty(p.shape, dtype=p.dtype, pin_memory=True)
+        do_h = torch.empty(dout.shape, dtype=dout.dtype, pin_memory=True)
+        v_h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+    except RuntimeError as exc:
+        return {"error": f"pinned host buffers unavailable: {exc}"}
+    p_h.copy_(p)
+    do_h.copy_(dout)
+    v_h.copy_(v)
+    lens_h = torch.from_numpy(lens).pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device=p.device)
+    torch.cuda.synchronize()
+    dp = gtms.device_pointer_of_host
+    args_c = (dp(p_h.data_ptr()), dp(do_h.data_ptr()), dp(v_h.data_ptr()), dp(ds_h.data_ptr()),
+              dp(lens_h.data_ptr()), w.B, w.M, w.S, w.head_dim, float(w.scale), w.dtype_code, status.data_ptr(),
+              stream.cuda_stream)
+    if fn(*args_c):
+        raise RuntimeError("gtms_attention_softmax_backward failed in the end-to-end loop")
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    rc = 0
+    for _ in range(args.e2e_steps):
+        rc |= fn(*args_c)
+    e.record(stream)
+    torch.cuda.synchronize()
+    if rc or int(status.item()):
+        raise RuntimeError("gtms_attention_softmax_backward failed in the end-to-end loop")
+    ms = s.elapsed_time(e) / args.e2e_steps
+    fb, _ = required_bytes(w, lens)
+    dense = w.B * w.M * w.S * w.S * w.elem_bytes
+    heads = 2 * w.B * w.M * w.S * w.head_dim * w.elem_bytes
+    return {"value": round((fb + heads) / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": fb - dense + heads + 4 * w.B, "d2h_bytes_per_step": dense,
+            "steps": args.e2e_steps,
+            "host_buffers": "pinned, mapped; the kernel reads kept P, dO, V from and writes dS to host memory "
+                            "over NVLink-C2C (no staging copy)"}
 
 
 def run_gpu(args, w, lens, rank, world, local_rank):
@@ -542,7 +702,10 @@ def main():
         if rank == 0:
             run_reference(args, w, lens)
         return
-    run_gpu(args, w, lens, rank, world, local_rank)
+    if w.head_dim > 0:
+        run_gpu_attention(args, w, lens, rank, world, local_rank)
+    else:
+        run_gpu(args, w, lens, rank, world, local_rank)
 
 
 if __name__ == "__main__":

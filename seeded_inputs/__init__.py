@@ -27,6 +27,9 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
   seq_len ~ U{8192..16384}, scale 0.125, and ``s32768_bf16`` --
   X[1,4,32768,32768], seq_len ~ U{16384..32768}: added measurement points for
   rows split over a cluster of CTAs.
+* ``attn_s2048_bf16`` -- the attention-backward step at the ``s2048_bf16``
+  shape: P the softmax of X[32,16,2048,2048] (bf16, variance 4,
+  seq_len ~ U{1024..2048}, scale 0.125), dO and V [32,16,2048,64] ~ N(0,1).
 * ``s1000_b2`` -- X[2,64,1000,1000], otherwise like ``s1000_b12``: a small
   stand-in for profiler captures.
 
@@ -61,6 +64,7 @@ class Workload:
     spike_value: float = 30.0
     backward: bool = True
     seed: int = 20261202
+    head_dim: int = 0                       # > 0: attention-backward step workload (dO, V of this width)
 
     @property
     def rows(self) -> int:
@@ -90,6 +94,9 @@ class Workload:
         dist = f"N(0,{self.x_std ** 2:g})"
         if self.spike_prob:
             dist += f"+{self.spike_prob:g}x{self.spike_value:g}"
+        if self.head_dim > 0:
+            return (f"dS from P=softmax(X[{self.B},{self.M},{self.S},{self.S}] {self.dtype} {dist} {lens} "
+                    f"scale={self.scale:g}), dO and V [{self.B},{self.M},{self.S},{self.head_dim}] N(0,1)")
         return (f"X[{self.B},{self.M},{self.S},{self.S}] {self.dtype} {dist} {lens} scale={self.scale:g} "
                 f"{'fwd+bwd' if self.backward else 'fwd'}")
 
@@ -112,6 +119,9 @@ WORKLOADS = {
                             seq_len_range=(8192, 16384), seed=20261210),
     "s32768_bf16": Workload("s32768_bf16", 1, 4, 32768, "bf16", 0.125, x_std=2.0,
                             seq_len_range=(16384, 32768), seed=20261211),
+    # attention-backward step (dS from P, dO, V) at the bf16 S = 2048 shape, head_dim 64
+    "attn_s2048_bf16": Workload("attn_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
+                                seq_len_range=(1024, 2048), seed=20261212, head_dim=64),
     # profiling stand-in for s1000_b12: same distribution, 2 of the 12 batches
     # (2 GB on the device), small enough for a multi-pass ncu capture
     "s1000_b2": Workload("s1000_b2", 2, 64, 1000, "f32", 1.0, seq_len_range=(500, 1000), seed=20261209),
@@ -172,6 +182,16 @@ def make_x(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.T
 def make_dy(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.Tensor:
     """Upstream gradient dY[B,M,S,S] ~ N(0,1) in the workload's dtype."""
     return _draw(w, device, 1, 1.0, False, max_chunk_elems)
+
+
+def make_head_operands(w: Workload, device="cpu"):
+    """dO and V [B, M, S, head_dim] ~ N(0,1) in the workload's dtype (attention-backward workloads)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(w.seed * 4 + 5)
+    shape = (w.B, w.M, w.S, w.head_dim)
+    dout = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(w.torch_dtype)
+    v = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(w.torch_dtype)
+    return dout, v
 
 
 def make_probs(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.Tensor:
