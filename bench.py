@@ -75,15 +75,23 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_sha():
+ATTN_SOURCES = ("gtms_attn_bwd.cu", "gtms_attn_bwd.cuh", "gtms_tcgen05.cuh", "gtms_kernels.cuh")
+
+
+def kernel_source_sha(kernel=""):
+    """Hash of the sources a kernel is compiled from: for the attention-backward
+    kernel its own files, for the softmax kernels every other file of csrc."""
     import glob
 
+    attn = kernel.startswith("gtms_attn")
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "masked_softmax_attention_gb300", "csrc", "*")))
-    for p in files:
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
-            h.update(f.read())
+    for p in sorted(glob.glob(os.path.join(ROOT, "masked_softmax_attention_gb300", "csrc", "*"))):
+        name = os.path.basename(p)
+        wanted = name in ATTN_SOURCES if attn else (name == "gtms_kernels.cuh" or name not in ATTN_SOURCES)
+        if wanted:
+            with open(p, "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -93,7 +101,7 @@ def recorded_traffic(kernel, workload):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    sha = kernel_source_sha()
+    sha = kernel_source_sha(kernel)
     with open(path) as f:
         for line in f:
             if not line.startswith("traffic "):
@@ -409,7 +417,7 @@ def run_gpu_attention(args, w, lens, rank, world, local_rank):
                                                        "required_bytes": nbytes, "achieved_gbs": round(gbs, 2),
                                                        "frac_of_peak": round(gbs / peak, 4)}},
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(gbs / peak, 4), "traffic": None,
+                         "frac": round(gbs / peak, 4), "traffic": recorded_traffic(kname, wr.name),
                          "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'recipe fallback 6.8 TB/s'})",
                          "algorithmic_bytes_per_launch": nbytes},
             "cpu_baseline": cpu, "e2e": e2e,

@@ -30,6 +30,8 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
 * ``attn_s2048_bf16`` -- the attention-backward step at the ``s2048_bf16``
   shape: P the softmax of X[32,16,2048,2048] (bf16, variance 4,
   seq_len ~ U{1024..2048}, scale 0.125), dO and V [32,16,2048,64] ~ N(0,1).
+* ``attn_s2048_b4`` -- ``attn_s2048_bf16`` with 4 batches: a profiler stand-in
+  (P and dS 537 MB each, still larger than L2).
 * ``s1000_b2`` -- X[2,64,1000,1000], otherwise like ``s1000_b12``: a small
   stand-in for profiler captures.
 
@@ -122,6 +124,9 @@ WORKLOADS = {
     # attention-backward step (dS from P, dO, V) at the bf16 S = 2048 shape, head_dim 64
     "attn_s2048_bf16": Workload("attn_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
                                 seq_len_range=(1024, 2048), seed=20261212, head_dim=64),
+    # profiling stand-in for attn_s2048_bf16: same distribution, 4 of the 32 batches
+    "attn_s2048_b4": Workload("attn_s2048_b4", 4, 16, 2048, "bf16", 0.125, x_std=2.0,
+                              seq_len_range=(1024, 2048), seed=20261212, head_dim=64),
     # profiling stand-in for s1000_b12: same distribution, 2 of the 12 batches
     # (2 GB on the device), small enough for a multi-pass ncu capture
     "s1000_b2": Workload("s1000_b2", 2, 64, 1000, "f32", 1.0, seq_len_range=(500, 1000), seed=20261209),
