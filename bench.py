@@ -405,7 +405,7 @@ def run_gpu_attention(args, w, lens, rank, world, local_rank):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, lens)
     if rank == 0:
-        kname = f"gtms_attn_dscores_kernel<{wr.dtype},d{wr.head_dim}>"
+        kname = f"gtms_attn_dscores_tma_kernel<{wr.dtype},d{wr.head_dim}>"   # device operands take the TMA kernel
         gbs = nbytes / (ms * 1e-3) / 1e9
         print(json.dumps({
             "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -470,7 +470,8 @@ def run_e2e_attention_host_resident(args, w, lens, p, dout, v, stream, fn):
             "h2d_bytes_per_step": fb - dense + heads + 4 * w.B, "d2h_bytes_per_step": dense,
             "steps": args.e2e_steps,
             "host_buffers": "pinned, mapped; the kernel reads kept P, dO, V from and writes dS to host memory "
-                            "over NVLink-C2C (no staging copy)"}
+                            "over NVLink-C2C (no staging copy); host operands take the cp.async kernel "
+                            f"gtms_attn_dscores_kernel<{w.dtype},d{w.head_dim}>"}
 
 
 def run_gpu(args, w, lens, rank, world, local_rank):

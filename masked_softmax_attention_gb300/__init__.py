@@ -286,6 +286,32 @@ def attention_softmax_backward(p, dout, v, seq_lens, scale: float = 1.0, out=Non
     return ds
 
 
+def attention_softmax_backward_host(p, dout, v, seq_lens, scale: float = 1.0, out=None, status=None, device=None):
+    """``attention_softmax_backward`` on pinned host tensors: the kernel reads P, dO, V and writes dS in host
+    memory (see ``forward_host``). ``status``, if given, is an int32 CUDA tensor of one element."""
+    import torch
+
+    for name, t in (("p", p), ("dout", dout), ("v", v), ("seq_lens", seq_lens)):
+        _check_pinned(name, t)
+    if p.dim() != 4 or p.shape[-1] != p.shape[-2] or dout.dim() != 4 or dout.shape != v.shape \
+            or dout.shape[:3] != p.shape[:3] or dout.dtype != p.dtype or v.dtype != p.dtype:
+        raise ValueError("p must be [B, M, S, S]; dout and v [B, M, S, d] of p's dtype")
+    if seq_lens.dtype != torch.int32 or seq_lens.shape != p.shape[:1]:
+        raise ValueError("seq_lens must be int32 [B]")
+    ds = torch.empty_like(p).pin_memory() if out is None else out
+    _check_pinned("out", ds)
+    B, M, S, _ = p.shape
+    stream = torch.cuda.current_stream(device).cuda_stream
+    dp = device_pointer_of_host
+    rc = gtms_attention_softmax_backward(dp(p.data_ptr()), dp(dout.data_ptr()), dp(v.data_ptr()),
+                                         dp(ds.data_ptr()), dp(seq_lens.data_ptr()), B, M, S, dout.shape[3],
+                                         float(scale), _dtype_code(p), None if status is None else status.data_ptr(),
+                                         stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_attention_softmax_backward", rc)
+    return ds
+
+
 def _check_pinned(name, t):
     if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous page-locked (pinned) CPU tensor")

@@ -63,9 +63,33 @@ extern template cudaError_t launch_attn_dscores<__half, 64>(const void*, const v
 extern template cudaError_t launch_attn_dscores<__half, 128>(const void*, const void*, const void*, void*,
                                                              const int32_t*, int64_t, int64_t, int64_t, float,
                                                              int32_t*, cudaStream_t);
+template <typename T, int D>
+cudaError_t launch_attn_dscores_tma(const void*, const void*, const void*, void*, const int32_t*, int64_t, int64_t,
+                                    int64_t, float, int32_t*, cudaStream_t);
+#define GTMS_EXTERN_ATTN_TMA(T, D)                                                                              \
+    extern template cudaError_t launch_attn_dscores_tma<T, D>(const void*, const void*, const void*, void*,     \
+                                                              const int32_t*, int64_t, int64_t, int64_t, float, \
+                                                              int32_t*, cudaStream_t);
+GTMS_EXTERN_ATTN_TMA(__nv_bfloat16, 64)
+GTMS_EXTERN_ATTN_TMA(__nv_bfloat16, 128)
+GTMS_EXTERN_ATTN_TMA(__half, 64)
+GTMS_EXTERN_ATTN_TMA(__half, 128)
+#undef GTMS_EXTERN_ATTN_TMA
 }  // namespace gtms
 
 namespace {
+
+// True for memory the CUDA runtime reports as device memory (not mapped host
+// memory, managed memory or an unknown pointer).
+bool in_device_memory(const void* ptr)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice;
+}
 
 int elem_bytes(int dtype)
 {
@@ -347,13 +371,25 @@ GTMS_EXPORT int gtms_attention_softmax_backward(const void* p, const void* dout,
         overlaps(ds, c.bytes, seq_lens, static_cast<uint64_t>(B) * 4) || (status && overlaps(ds, c.bytes, status, 4)))
         return GTMS_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Operands in device memory take the TMA-fed persistent kernel; any in
+    // mapped host memory, the kernel that copies with cp.async.
+    const bool tma = in_device_memory(p) && in_device_memory(dout) && in_device_memory(v) && in_device_memory(ds);
     cudaError_t e;
-    if (dtype == GTMS_BF16)
-        e = head_dim == 64 ? gtms::launch_attn_dscores<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
-                           : gtms::launch_attn_dscores<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
-    else
-        e = head_dim == 64 ? gtms::launch_attn_dscores<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
-                           : gtms::launch_attn_dscores<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+    if (dtype == GTMS_BF16) {
+        if (tma)
+            e = head_dim == 64 ? gtms::launch_attn_dscores_tma<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
+                               : gtms::launch_attn_dscores_tma<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+        else
+            e = head_dim == 64 ? gtms::launch_attn_dscores<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
+                               : gtms::launch_attn_dscores<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+    } else {
+        if (tma)
+            e = head_dim == 64 ? gtms::launch_attn_dscores_tma<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
+                               : gtms::launch_attn_dscores_tma<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+        else
+            e = head_dim == 64 ? gtms::launch_attn_dscores<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
+                               : gtms::launch_attn_dscores<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GTMS_ERR_CUDA;

@@ -139,15 +139,18 @@ __device__ __forceinline__ void store_ds_tile(const uint8_t* stage, const TileLa
 }
 
 // Zero-fill columns [c_from, S) of rows [row0, row1) of one [S, S] slice with
-// 16-byte stores, the CTA's threads walking the region's units in row-major
-// order (S % 8 == 0).
+// 16-byte stores, `nthreads` threads (this one is number t) walking the
+// region's units in row-major order (S % 8 == 0). The lines are marked to
+// leave L2 first: nothing reads them again.
 template <typename T>
-__device__ __forceinline__ void zero_region(T* slice, int32_t S, int32_t row0, int32_t row1, int32_t c_from)
+__device__ __forceinline__ void zero_region(T* slice, int32_t S, int32_t row0, int32_t row1, int32_t c_from,
+                                            int t = threadIdx.x, int nthreads = kAttnThreads)
 {
     const int32_t units = (S - c_from) / 8;   // per row
     if (units <= 0 || row1 <= row0)
         return;
-    int32_t r = row0, u = threadIdx.x;
+    const uint64_t pol = tc::policy_evict_first();
+    int32_t r = row0, u = t;
     while (u >= units) {
         u -= units;
         ++r;
@@ -155,8 +158,8 @@ __device__ __forceinline__ void zero_region(T* slice, int32_t S, int32_t row0, i
     uint4* row_ptr = reinterpret_cast<uint4*>(slice + static_cast<int64_t>(r) * S + c_from);
     const int32_t row_units = S / 8;
     while (r < row1) {
-        row_ptr[u] = make_uint4(0u, 0u, 0u, 0u);
-        u += kAttnThreads;
+        tc::st_global_zero16(row_ptr + u, pol);
+        u += nthreads;
         while (u >= units) {
             u -= units;
             ++r;

@@ -1,0 +1,490 @@
+// gtms_attn_tma.cuh -- the fused attention-backward step (dS from P, dO, V; see
+// gtms_attn_bwd.cuh for the arithmetic) as a warp-specialised, TMA-fed,
+// persistent kernel for operands in device memory.
+//
+// "ops(8): self-attention 的 CUDA 实现及优化 (下)", section 2.1:
+//   dP = dO V^T,  dS = scale * P * (dP - rowsum(dP * P))  over the kept set c <= r < L.
+//
+// One CTA per SM walks the (slice, 128-row block) work items (see attn_item
+// for their order). Its warps:
+//   producer (1 lane)  TMA loads into a ring of stages: per tile iteration the
+//                      V tile (16 boxes of 8 columns, no swizzle: K-adjacent
+//                      core matrices 2 KB apart) and the P tile (two 64-column
+//                      boxes, 128-byte swizzle); once per work item the dO rows
+//                      (two buffers, so the next item's can land early);
+//   MMA (1 lane)       tcgen05.mma dP tile = dO . V^T into one of two
+//                      tensor-memory accumulators, committed to mbarriers that
+//                      hand the accumulator to the epilogue and the V tile back
+//                      to the producer;
+//   epilogue (16 warps) warp w reads lanes 32 (w % 4) .. + 31 (its rows) and
+//                      columns 32 (w / 4) .. + 31 of the accumulator, and forms
+//                      the row sums (pass 1) or writes dS over P in the stage
+//                      (pass 2);
+//   store (1 lane)     TMA-stores each finished dS tile (rows past the tensor
+//                      are dropped by the TMA unit) and returns the stage;
+//   zero (2 warps)     zero-fill each block's columns right of the diagonal
+//                      tile, and whole padded row blocks.
+// Every hand-off is an mbarrier; every wait is bounded. If a wait runs out, the
+// kernel ORs 1 into the caller's status word, every role leaves its loop, the
+// outstanding copies and MMAs are waited for (bounded) and the tensor memory is
+// freed.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gtms_attn_bwd.cuh"
+#include "gtms_tcgen05.cuh"
+
+namespace gtms {
+
+constexpr int kTmaEpiWarps = 16;                          // 4 lane quarters x 4 column quarters
+constexpr int kWarpProducer = 16, kWarpMma = 17, kWarpStore = 18, kWarpZero0 = 19, kZeroWarps = 2;
+constexpr int kTmaThreads = 32 * (kWarpZero0 + kZeroWarps);
+
+template <int D>
+struct AttnTma {
+    static constexpr int NS = D == 64 ? 3 : 2;                      // stages in the ring
+    static constexpr uint32_t op = kAttnRows * D * 2;               // 128 rows of dO or V
+    static constexpr uint32_t off_p = 0;                            // NS P / dS tiles (1024-aligned)
+    static constexpr uint32_t off_v = NS * kAttnPTileBytes;         // NS V tiles
+    static constexpr uint32_t off_do = off_v + NS * op;             // 2 dO tiles
+    static constexpr uint32_t off_red = off_do + 2 * op;            // 8 x 128 floats: row-sum exchange
+    static constexpr uint32_t bytes = off_red + 8 * kAttnRows * 4 + 1024;   // + slack to align the base
+    static constexpr uint32_t lbo = kAttnRows * 16;                 // K-adjacent core matrices (one 8-column box)
+    static constexpr uint32_t sbo = 128;                            // row-adjacent core matrices
+    static constexpr uint32_t stage_tx = op + kAttnPTileBytes;      // bytes per tile iteration
+};
+
+struct AttnShared {
+    uint64_t full[3], empty[3], dsready[3];   // per stage
+    uint64_t tfull[2], tempty[2];             // per accumulator
+    uint64_t dofull[2], doempty[2];           // per dO buffer
+    uint64_t red_in, red_out;                 // row-sum exchange between the column halves
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+__device__ __forceinline__ bool attn_aborted(const AttnShared& sh)
+{
+    return *reinterpret_cast<const volatile int*>(&sh.abort_flag) != 0;
+}
+
+__device__ __forceinline__ void attn_abort(AttnShared& sh, int32_t* status)
+{
+    *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
+    if (status)
+        atomicOr(status, 1);
+}
+
+// All 32 lanes wait; the verdict is the warp's (so that warp-collective
+// instructions that follow stay converged).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity)
+{
+    return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, kAttnWaitLimit)) != 0;
+}
+
+struct AttnItem {
+    int64_t slice;
+    int32_t r0, L, n_tiles;
+};
+
+// Work item `item`: the slices are taken in groups of `group` (the last group
+// may be smaller); inside a group, row-block-major with the costliest row
+// blocks first: row block nrb - 1 - j / k of slice group_start + j % k, for
+// item = group_start * nrb + j and k the group's size. A CTA takes items
+// blockIdx.x + n * gridDim.x, so every CTA meets every row block about equally
+// often (the CTAs finish together), and at any time the CTAs work on the rows
+// of one group of slices only (few pages of P and dS in use at once).
+__device__ __forceinline__ AttnItem attn_item(int64_t item, int64_t n_slices, int64_t group, int32_t nrb, int32_t M,
+                                              int32_t S, const int32_t* __restrict__ seq_lens)
+{
+    AttnItem it;
+    const int64_t gi = item / (group * nrb), j = item % (group * nrb);
+    const int64_t k = n_slices - gi * group < group ? n_slices - gi * group : group;
+    it.slice = gi * group + j % k;
+    it.r0 = (nrb - 1 - static_cast<int32_t>(j / k)) * kAttnRows;
+    int32_t L = __ldg(seq_lens + static_cast<int32_t>(it.slice / M));
+    it.L = L < 0 ? 0 : (L > S ? S : L);
+    it.n_tiles = it.r0 < it.L ? it.r0 / kAttnRows + 1 : 0;   // 0: padded block, no GEMM
+    return it;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_ds,
+                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                             T* dS, const int32_t* __restrict__ seq_lens, int32_t M, int32_t S, int32_t nrb,
+                             int64_t n_slices, int64_t group, float scale, int32_t* status)
+{
+    using IO = Pairs<T>;
+    using TL = AttnTma<D>;
+    constexpr int NS = TL::NS;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ AttnShared sh;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n_items = n_slices * nrb;
+    const uint32_t raw_u32 = tc::smem_u32(smem_raw);
+    const uint32_t base = (raw_u32 + 1023u) & ~1023u;              // 1024-aligned for the 128-byte swizzle
+    uint8_t* smem = smem_raw + (base - raw_u32);
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            tc::mbar_init(&sh.full[s], 1);
+            tc::mbar_init(&sh.empty[s], 1 + kTmaEpiWarps);   // MMA commit + (16 epilogue warps or the store lane x 16)
+            tc::mbar_init(&sh.dsready[s], kTmaEpiWarps);
+        }
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&sh.tfull[a], 1);
+            tc::mbar_init(&sh.tempty[a], kTmaEpiWarps);
+            tc::mbar_init(&sh.dofull[a], 1);
+            tc::mbar_init(&sh.doempty[a], 1);
+        }
+        tc::mbar_init(&sh.red_in, 3 * kAttnRows);   // the threads of column quarters 1..3
+        tc::mbar_init(&sh.red_out, kAttnRows);      // the threads of column quarter 0
+        sh.abort_flag = 0;
+    }
+    if (warp == kWarpMma) {
+        __syncwarp();
+        tc::tmem_alloc<2 * kAttnRows>(&sh.tmem_slot);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = sh.tmem_slot;
+
+    if (warp == kWarpProducer) {
+        if (lane == 0) {
+            uint32_t g = 0, itm = 0;
+            bool ok = true;
+            for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
+                if (it.n_tiles == 0)
+                    continue;
+                const int32_t z = static_cast<int32_t>(it.slice);
+                const uint32_t p = itm & 1u;
+                ok = tc::mbar_wait(&sh.doempty[p], ((itm >> 1) & 1u) ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                if (!ok)
+                    break;
+                tc::mbar_arrive_expect_tx(&sh.dofull[p], TL::op);
+                for (int kc = 0; kc < D / 8; ++kc)
+                    tc::tma_load_3d(base + TL::off_do + p * TL::op + kc * TL::lbo, &tm_do, kc * 8, it.r0, z, &sh.dofull[p]);
+                for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
+                    const uint32_t s = g % NS, ph = (g / NS) & 1u;
+                    const int32_t tc0 = (i < it.n_tiles ? i : i - it.n_tiles) * kAttnRows;
+                    ok = tc::mbar_wait(&sh.empty[s], ph ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                    if (!ok)
+                        break;
+                    tc::mbar_arrive_expect_tx(&sh.full[s], TL::stage_tx);
+                    for (int kc = 0; kc < D / 8; ++kc)
+                        tc::tma_load_3d(base + TL::off_v + s * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z, &sh.full[s]);
+                    const uint32_t pt = base + TL::off_p + s * kAttnPTileBytes;
+                    // Pass 1 keeps the P tile in L2 for pass 2, which is its last read.
+                    const uint64_t pol = i < it.n_tiles ? tc::policy_evict_last() : tc::policy_evict_first();
+                    tc::tma_load_3d(pt, &tm_p, tc0, it.r0, z, &sh.full[s], pol);
+                    tc::tma_load_3d(pt + kAttnRows * 128, &tm_p, tc0 + 64, it.r0, z, &sh.full[s], pol);
+                }
+                ++itm;
+            }
+            if (!ok) {
+                attn_abort(sh, status);
+                // Let the copies already issued land before the CTA can exit.
+                for (uint32_t k = 0; k < static_cast<uint32_t>(NS) && k < g; ++k) {
+                    const uint32_t gk = g - 1 - k;
+                    tc::mbar_wait(&sh.full[gk % NS], (gk / NS) & 1u, kAttnWaitLimit);
+                }
+                if (itm > 0)
+                    tc::mbar_wait(&sh.dofull[(itm - 1) & 1u], ((itm - 1) >> 1) & 1u, kAttnWaitLimit);
+            }
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_f16<T>(kAttnRows, kAttnRows);
+            uint32_t g = 0, itm = 0;
+            bool ok = true, issued = false;
+            for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
+                if (it.n_tiles == 0)
+                    continue;
+                const uint32_t p = itm & 1u;
+                ok = tc::mbar_wait(&sh.dofull[p], (itm >> 1) & 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                if (!ok)
+                    break;
+                const uint32_t a_base = base + TL::off_do + p * TL::op;
+                for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
+                    const uint32_t s = g % NS, ph = (g / NS) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
+                    ok = tc::mbar_wait(&sh.tempty[acc], pha ^ 1u, kAttnWaitLimit) &&
+                         tc::mbar_wait(&sh.full[s], ph, kAttnWaitLimit) && !attn_aborted(sh);
+                    if (!ok)
+                        break;
+                    tc::fence_after_sync();
+                    const uint32_t b_base = base + TL::off_v + s * TL::op;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tc::mma_f16(tmem + acc * kAttnRows, tc::smem_desc(a_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo),
+                                    tc::smem_desc(b_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo), idesc, ks > 0 ? 1u : 0u);
+                    tc::commit(&sh.tfull[acc]);
+                    tc::commit(&sh.empty[s]);
+                    issued = true;
+                }
+                if (!ok)
+                    break;
+                tc::commit(&sh.doempty[p]);
+                ++itm;
+            }
+            if (!ok)
+                attn_abort(sh, status);
+            if (issued) {   // the last MMAs must complete before the tensor memory is freed
+                const uint32_t gl = g - 1;
+                tc::mbar_wait(&sh.tfull[gl & 1u], (gl >> 1) & 1u, kAttnWaitLimit);
+            }
+        }
+    } else if (warp == kWarpStore) {
+        if (lane == 0) {
+            uint32_t g = 0, ds_par = 0;
+            bool ok = true;
+            for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
+                const int32_t z = static_cast<int32_t>(it.slice);
+                for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
+                    if (i < it.n_tiles)
+                        continue;
+                    const uint32_t s = g % NS;
+                    ok = tc::mbar_wait(&sh.dsready[s], (ds_par >> s) & 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                    if (!ok)
+                        break;
+                    ds_par ^= 1u << s;
+                    const int32_t tc0 = (i - it.n_tiles) * kAttnRows;
+                    const uint32_t pt = base + TL::off_p + s * kAttnPTileBytes;
+                    const uint64_t pol = tc::policy_evict_first();   // dS is not read again here
+                    tc::tma_store_3d(&tm_ds, tc0, it.r0, z, pt, pol);
+                    if (tc0 + 64 < S)   // (a box wholly past the last column is not issued)
+                        tc::tma_store_3d(&tm_ds, tc0 + 64, it.r0, z, pt + kAttnRows * 128, pol);
+                    tc::bulk_commit();
+                    tc::bulk_wait_read_all();
+                    tc::mbar_arrive(&sh.empty[s], kTmaEpiWarps);
+                }
+            }
+            if (!ok)
+                attn_abort(sh, status);
+            tc::bulk_wait_all();
+        }
+    } else if (warp >= kWarpZero0) {
+        // Zero-fill warps: columns right of the diagonal tile, whole padded row blocks.
+        const int zt = tid - kWarpZero0 * 32;
+        for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+            if (attn_aborted(sh))
+                break;
+            const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
+            const int32_t r_end = it.r0 + kAttnRows < S ? it.r0 + kAttnRows : S;
+            const int32_t c_from = it.n_tiles * kAttnRows < S ? it.n_tiles * kAttnRows : S;
+            zero_region(dS + it.slice * static_cast<int64_t>(S) * S, S, it.r0, r_end, c_from, zt, kZeroWarps * 32);
+        }
+    } else {
+        // Epilogue warps 0..15: rows 32 (w % 4) + lane, columns 32 (w / 4) .. + 31 of each tile.
+        const int quarter = warp & 3, colq = warp >> 2;
+        const int row = quarter * 32 + lane;
+        float* red = reinterpret_cast<float*>(smem + TL::off_red);
+        const uint32_t row_off = TL::off_p + (colq >> 1) * (kAttnRows * 128) + row * 128;
+        const int chunk0 = (colq & 1) * 4, rx = row & 7;
+        uint32_t g = 0, itm = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
+            if (it.n_tiles == 0)
+                continue;
+            const int32_t r = it.r0 + row;
+            const bool live = r < it.L;
+            float dot_hi = 0.0f, dot_lo = 0.0f, dh = 0.0f, dl = 0.0f;
+            for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
+                const bool pass2 = i >= it.n_tiles;
+                const int32_t tc0 = (pass2 ? i - it.n_tiles : i) * kAttnRows;
+                // Kept elements of this thread's 32 columns: the first `kept` of them.
+                const int32_t lim = live ? r - (tc0 + colq * 32) + 1 : 0;
+                const int kept = lim < 0 ? 0 : (lim > 32 ? 32 : lim);
+                const uint32_t s = g % NS, ph = (g / NS) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
+                ok = warp_wait(&sh.tfull[acc], pha) && !attn_aborted(sh);
+                if (!ok)
+                    break;
+                tc::fence_after_sync();
+                float dp[32];
+                tc::tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAttnRows + colq * 32, dp);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(&sh.tempty[acc]);
+                ok = warp_wait(&sh.full[s], ph);   // the P tile (landed before the MMA ran)
+                if (!ok)
+                    break;
+                uint8_t* p_row = smem + row_off + s * kAttnPTileBytes;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4* cell = reinterpret_cast<uint4*>(p_row + (((chunk0 + u) ^ rx) << 4));
+                    const int n_in = kept - u * 8;   // kept elements in this unit, if < 8
+                    if (n_in <= 0) {                  // nothing kept in this unit
+                        if (pass2)
+                            *cell = make_uint4(0u, 0u, 0u, 0u);
+                        continue;
+                    }
+                    const uint4 raw = *cell;          // (kept columns lie inside the tensor)
+                    Unit16 pu{{raw.x, raw.y, raw.z, raw.w}};
+                    if (n_in < 8) {   // masked P and dP read as +0.0 (dP may be infinite where P is masked)
+                        IO::clear_outside(pu, 0, n_in);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dp[u * 8 + e] = e < n_in ? dp[u * 8 + e] : 0.0f;
+                    }
+                    if (!pass2) {
+                        float2 a2 = __fmul2_rn(IO::get(pu, 0), make_float2(dp[u * 8], dp[u * 8 + 1]));
+#pragma unroll
+                        for (int q = 1; q < 4; ++q)
+                            a2 = __ffma2_rn(IO::get(pu, q), make_float2(dp[u * 8 + 2 * q], dp[u * 8 + 2 * q + 1]), a2);
+                        float sum, err;
+                        two_sum(dot_hi, __fadd_rn(a2.x, a2.y), sum, err);
+                        dot_hi = sum;
+                        dot_lo = __fadd_rn(dot_lo, err);
+                    } else {
+                        const float2 ndh = make_float2(-dh, -dh), ndl = make_float2(-dl, -dl);
+                        const float2 sc = make_float2(scale, scale);
+                        Unit16 o;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 gq = make_float2(dp[u * 8 + 2 * q], dp[u * 8 + 2 * q + 1]);
+                            const float2 t = __fadd2_rn(__fadd2_rn(gq, ndh), ndl);
+                            IO::put(o, q, __fmul2_rn(__fmul2_rn(IO::get(pu, q), t), sc));
+                        }
+                        if (n_in < 8)
+                            IO::clear_outside(o, 0, n_in);   // masked entries are +0.0 bits
+                        *cell = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+                    }
+                }
+                if (!pass2) {
+                    __syncwarp();
+                    if (lane == 0)
+                        tc::mbar_arrive(&sh.empty[s]);
+                    if (i == it.n_tiles - 1) {   // merge the four column quarters' row sums
+                        const uint32_t rp = itm & 1u;
+                        if (colq != 0) {
+                            red[(colq - 1) * 2 * kAttnRows + row] = dot_hi;
+                            red[(colq - 1) * 2 * kAttnRows + kAttnRows + row] = dot_lo;
+                            tc::mbar_arrive(&sh.red_in);
+                            ok = warp_wait(&sh.red_out, rp);
+                            dh = red[6 * kAttnRows + row];
+                            dl = red[7 * kAttnRows + row];
+                        } else {
+                            ok = warp_wait(&sh.red_in, rp);
+                            float hi = dot_hi, lo = dot_lo;
+#pragma unroll
+                            for (int k = 0; k < 3; ++k) {
+                                float sum, err;
+                                two_sum(hi, red[k * 2 * kAttnRows + row], sum, err);
+                                hi = sum;
+                                lo = __fadd_rn(__fadd_rn(lo, red[k * 2 * kAttnRows + kAttnRows + row]), err);
+                            }
+                            dh = __fadd_rn(hi, lo);
+                            dl = __fsub_rn(lo, __fsub_rn(dh, hi));
+                            red[6 * kAttnRows + row] = dh;
+                            red[7 * kAttnRows + row] = dl;
+                            tc::mbar_arrive(&sh.red_out);
+                        }
+                        if (!ok)
+                            break;
+                    }
+                } else {
+                    tc::fence_smem_for_async();   // dS in the stage, visible to the TMA store
+                    __syncwarp();
+                    if (lane == 0)
+                        tc::mbar_arrive(&sh.dsready[s]);
+                }
+            }
+            ++itm;
+        }
+        if (!ok && lane == 0)
+            attn_abort(sh, status);
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == kWarpMma) {
+        __syncwarp();
+        tc::tmem_free<2 * kAttnRows>(tmem);
+    }
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+using TensorMapEncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                       const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                       CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline TensorMapEncodeFn tensor_map_encoder()
+{
+    static TensorMapEncodeFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<TensorMapEncodeFn>(f);
+    }();
+    return fn;
+}
+
+// 3-D map of 16-bit elements [n2][n1][n0] (n0 contiguous) with box {b0, b1, 1}.
+inline bool encode_map_3d(CUtensorMap* map, const void* ptr, uint64_t n0, uint64_t n1, uint64_t n2, uint32_t b0,
+                          uint32_t b1, CUtensorMapSwizzle swz)
+{
+    const TensorMapEncodeFn enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[3] = {n0, n1, n2};
+    const cuuint64_t strides[2] = {n0 * 2, n0 * n1 * 2};
+    const cuuint32_t box[3] = {b0, b1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Persistent launch: one CTA per SM (at most one per work item).
+template <typename T, int D>
+cudaError_t launch_attn_dscores_tma(const void* P, const void* dO, const void* V, void* dS, const int32_t* seq_lens,
+                                    int64_t B, int64_t M, int64_t S, float scale, int32_t* status, cudaStream_t st)
+{
+    const uint64_t slices = static_cast<uint64_t>(B) * M;
+    CUtensorMap tm_p, tm_ds, tm_v, tm_do;
+    if (!encode_map_3d(&tm_p, P, S, S, slices, 64, kAttnRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_3d(&tm_ds, dS, S, S, slices, 64, kAttnRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_map_3d(&tm_v, V, D, S, slices, 8, kAttnRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_3d(&tm_do, dO, D, S, slices, 8, kAttnRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    constexpr int smem = static_cast<int>(AttnTma<D>::bytes);
+    auto* kern = gtms_attn_dscores_tma_kernel<T, D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    const int32_t nrb = static_cast<int32_t>((S + kAttnRows - 1) / kAttnRows);
+    const int64_t n_items = static_cast<int64_t>(slices) * nrb;
+    const int nsm = sm_count();
+    if (nsm <= 0)
+        return cudaErrorUnknown;
+    const int64_t grid = n_items < nsm ? n_items : nsm;
+    const int64_t group = (4 * grid + nrb - 1) / nrb;   // slices whose items make about 4 per CTA
+    kern<<<static_cast<unsigned>(grid), kTmaThreads, smem, st>>>(tm_p, tm_ds, tm_v, tm_do, static_cast<T*>(dS),
+                                                                 seq_lens, static_cast<int32_t>(M),
+                                                                 static_cast<int32_t>(S), nrb,
+                                                                 static_cast<int64_t>(slices), group, scale, status);
+    return cudaGetLastError();
+}
+
+}  // namespace gtms

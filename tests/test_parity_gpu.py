@@ -636,3 +636,65 @@ def test_attention_softmax_backward_in_place_and_masked_p_not_read(dev):
     got = gtms.attention_softmax_backward(p_nan, dout.to(dev), v.to(dev), lens_d, w.scale, out=p_nan)
     torch.cuda.synchronize()
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+def test_attention_softmax_backward_many_items_per_cta(dev):
+    """512 (slice, row block) items: each persistent CTA takes several, so the stage ring, both
+    tensor-memory accumulators and both dO buffers wrap around many times."""
+    B, M, S, d, dtype = 4, 16, 1024, 64, "bf16"
+    w, p_bits, dout, v = _attn_case(dev, B, M, S, d, dtype, (1024, 700, 513, 1), seed=91)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    p_d = from_bits(p_bits, dtype, "cpu").view(B, M, S, S).to(dev)
+    ds = torch.full_like(p_d, float("nan"))
+    gtms.attention_softmax_backward(p_d, dout.to(dev), v.to(dev), torch.from_numpy(si.seq_lens(w)).to(dev),
+                                    w.scale, out=ds, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _attn_check(w, d, p_bits, dout, v, ds, "B=4 M=16 S=1024")
+
+
+@pytest.mark.parametrize("S,d,dtype,lens", [(1000, 64, "bf16", (1000, 513)), (384, 128, "f16", (300, 384))])
+def test_attention_softmax_backward_host_resident(dev, S, d, dtype, lens):
+    """Operands in mapped pinned host memory (the kernel that copies with cp.async)."""
+    B, M = 2, 2
+    w, p_bits, dout, v = _attn_case(dev, B, M, S, d, dtype, lens, seed=S + 7)
+    p_h = from_bits(p_bits, dtype, "cpu").view(B, M, S, S).pin_memory()
+    ds_h = torch.full_like(p_h, float("nan")).pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    gtms.attention_softmax_backward_host(p_h, dout.pin_memory(), v.pin_memory(),
+                                         torch.from_numpy(si.seq_lens(w)).pin_memory(), w.scale, out=ds_h,
+                                         status=status, device=dev)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _attn_check(w, d, p_bits, dout, v, ds_h, f"host S={S} d={d} {dtype}")
+
+
+def test_attention_softmax_backward_full_size_sampled(dev):
+    """The benchmark's workload (P[32,16,2048,2048] bf16, head dim 64) in the benchmark's launch: masked bits
+    zero everywhere; sampled slices, whose P is the oracle's own forward, element-wise against the oracle."""
+    w = si.WORKLOADS["attn_s2048_bf16"]
+    B, M, S, d = w.B, w.M, w.S, w.head_dim
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    x = si.make_x(w, dev)
+    p = gtms.forward(x, lens_d, w.scale)
+    dout, v = si.make_head_operands(w, dev)
+    slices = si.sample_slices(w, 4)
+    p_ref = {}
+    for b, m in slices:
+        xs = to_bits(x[b, m], w.dtype).reshape(1, 1, S, S)
+        p_ref[(b, m)] = oracle_forward_bits(xs, lens[b:b + 1], 1, 1, S, w.scale, w.dtype)
+        p[b, m].copy_(from_bits(p_ref[(b, m)], w.dtype, "cpu").view(S, S))
+    del x
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ds = gtms.attention_softmax_backward(p, dout, v, lens_d, w.scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert masked_bits_all_zero(ds, lens_d, w.dtype)
+    assert bool(torch.isfinite(ds).all())
+    for b, m in slices:
+        ws = si.custom("attn_slice", 1, 1, S, w.dtype, w.scale, seq_lens=(int(lens[b]),))
+        _attn_check(ws, d, p_ref[(b, m)], dout[b, m].reshape(1, 1, S, d).cpu(), v[b, m].reshape(1, 1, S, d).cpu(),
+                    ds[b, m].reshape(1, 1, S, S), f"full size slice ({b},{m})")
+    del p, ds, dout, v
+    torch.cuda.empty_cache()
