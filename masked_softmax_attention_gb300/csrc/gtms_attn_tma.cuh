@@ -8,10 +8,12 @@
 // One CTA per SM walks the (slice, 128-row block) work items (see attn_item
 // for their order). Its warps:
 //   producer (1 lane)  TMA loads into a ring of stages: per tile iteration the
-//                      V tile (16 boxes of 8 columns, no swizzle: K-adjacent
-//                      core matrices 2 KB apart) and the P tile (two 64-column
+//                      V tile (8-column boxes, no swizzle: K-adjacent core
+//                      matrices 2 KB apart) and the P tile (two 64-column
 //                      boxes, 128-byte swizzle); once per work item the dO rows
-//                      (two buffers, so the next item's can land early);
+//                      (two buffers, so the next item's can land early); and
+//                      an L2 prefetch of the next P tile before it waits for
+//                      a free stage;
 //   MMA (1 lane)       tcgen05.mma dP tile = dO . V^T into one of two
 //                      tensor-memory accumulators, committed to mbarriers that
 //                      hand the accumulator to the epilogue and the V tile back
@@ -42,6 +44,9 @@ namespace gtms {
 constexpr int kTmaEpiWarps = 16;                          // 4 lane quarters x 4 column quarters
 constexpr int kWarpProducer = 16, kWarpMma = 17, kWarpStore = 18, kWarpZero0 = 19, kZeroWarps = 2;
 constexpr int kTmaThreads = 32 * (kWarpZero0 + kZeroWarps);
+// Tile iterations by which the L2 prefetch of P runs ahead of the TMA loads
+// (measured on GB300: 0-2 is best, 6 and more lose to L2 thrashing).
+constexpr uint32_t kPrefetchAhead = 1;
 
 template <int D>
 struct AttnTma {
@@ -159,6 +164,23 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
         if (lane == 0) {
             uint32_t g = 0, itm = 0;
             bool ok = true;
+            // A second cursor walks the same iterations kPrefetchAhead ahead of the
+            // loads and prefetches the P tiles of pass 1 into L2, so that the TMA
+            // loads into the ring find them there.
+            const uint64_t pol_keep = tc::policy_evict_last();
+            int64_t pf_item = blockIdx.x;
+            AttnItem pf{};
+            int32_t pf_i = 0;
+            uint32_t pf_g = 0;
+            auto pf_seek = [&]() {   // the cursor's next work item that has tiles
+                for (; pf_item < n_items; pf_item += gridDim.x) {
+                    pf = attn_item(pf_item, n_slices, group, nrb, M, S, seq_lens);
+                    if (pf.n_tiles > 0)
+                        return true;
+                }
+                return false;
+            };
+            bool pf_live = pf_seek();
             for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
                 const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
                 if (it.n_tiles == 0)
@@ -174,6 +196,20 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
                     const uint32_t s = g % NS, ph = (g / NS) & 1u;
                     const int32_t tc0 = (i < it.n_tiles ? i : i - it.n_tiles) * kAttnRows;
+                    while (pf_live && pf_g <= g + kPrefetchAhead) {
+                        if (pf_i < pf.n_tiles) {
+                            const int32_t zf = static_cast<int32_t>(pf.slice);
+                            tc::tma_prefetch_3d(&tm_p, pf_i * kAttnRows, pf.r0, zf, pol_keep);
+                            if (pf_i * kAttnRows + 64 < S)
+                                tc::tma_prefetch_3d(&tm_p, pf_i * kAttnRows + 64, pf.r0, zf, pol_keep);
+                        }
+                        ++pf_g;
+                        if (++pf_i == 2 * pf.n_tiles) {
+                            pf_i = 0;
+                            pf_item += gridDim.x;
+                            pf_live = pf_seek();
+                        }
+                    }
                     ok = tc::mbar_wait(&sh.empty[s], ph ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
                     if (!ok)
                         break;

@@ -199,6 +199,14 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, int32_t x, int32_
                  :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(src), "l"(pol) : "memory");
 }
 
+// TMA: prefetch the box of a 3-D tensor map at (x, y, z) into L2 (no shared
+// memory, no completion signal), under an L2 cache policy.
+__device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t x, int32_t y, int32_t z, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;"
+                 :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "l"(pol) : "memory");
+}
+
 // 16 zero bytes to global memory under an L2 cache policy.
 __device__ __forceinline__ void st_global_zero16(void* p, uint64_t pol)
 {
