@@ -239,9 +239,24 @@ def oracle_step(ws, xb, dyb, threads):
         oracle.round_to(dx, ws.dtype_code)
 
 
+def cpu_model():
+    """The host CPU's model name (Linux /proc/cpuinfo; Arm hosts report no name, so the part number)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return None
+    for key in ("model name", "Model Name", "CPU part"):
+        for line in info.splitlines():
+            if line.startswith(key):
+                return line.split(":", 1)[1].strip()
+    return None
+
+
 def cpu_baseline(w, lens, budget_s=12.0):
     """The oracle as it stands, on the host cores, over a bounded sample of the
-    workload: groups of (b, m) slices until about budget_s of wall time."""
+    workload: groups of (b, m) slices until about budget_s of wall time, on all
+    cores; then one group on a single thread."""
     threads = os.cpu_count() or 1
     group = max(1, min(16, w.B * w.M))
     done_slices, total_bytes, total_s, groups = 0, 0, 0.0, 0
@@ -254,7 +269,12 @@ def cpu_baseline(w, lens, budget_s=12.0):
         total_bytes += step_bytes(ws, ws.fixed_seq_lens)
         done_slices += group
         groups += 1
+    ws, xb, dyb = oracle_sample(w, lens, [(b % w.B, 0) for b in range(min(4, w.B * w.M))])
+    t0 = time.perf_counter()
+    oracle_step(ws, xb, dyb, 1)
+    single = step_bytes(ws, ws.fixed_seq_lens) / (time.perf_counter() - t0) / 1e9
     return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "value_1_thread": round(single, 4), "cpu_model": cpu_model(),
             "sample": f"{done_slices} (b,m) slices of {w.name} (S={w.S}, the workload's seq_lens and value "
                       f"distribution, drawn on the CPU) in {groups} groups: {oracle_step_name(w)}, "
                       f"{total_s:.2f} s wall on {threads} threads"}
@@ -541,6 +561,7 @@ def run_gpu(args, w, lens, rank, world, local_rank):
     total_ms = start.elapsed_time(end)
     fwd_ms = statistics.fmean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.fmean(e[1].elapsed_time(e[2]) for e in ev) if wr.backward else 0.0
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     ms_step = max_over_ranks(total_ms / K, dist, dev)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
 
@@ -579,6 +600,7 @@ def run_gpu(args, w, lens, rank, world, local_rank):
                 "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
                 "config": workload_config(w, lens), "pct_hbm_peak": round(100 * (value / world) / peak, 2),
+                "ms_per_step_median": round(statistics.median(step_ms), 5), "ms_per_step_min": round(min(step_ms), 5),
                 "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_staged": e2e_staged,
                 "gpu_launches": K * (2 if wr.backward else 1), "clocks": clocks,
                 "impl": "gtms"}

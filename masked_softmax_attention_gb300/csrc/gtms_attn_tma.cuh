@@ -7,17 +7,18 @@
 //
 // One CTA per SM walks the (slice, 128-row block) work items (see attn_item
 // for their order). Its warps:
-//   producer (1 lane)  TMA loads into a ring of stages: per tile iteration the
-//                      V tile (8-column boxes, no swizzle: K-adjacent core
-//                      matrices 2 KB apart) and the P tile (two 64-column
-//                      boxes, 128-byte swizzle); once per work item the dO rows
+//   producer (1 lane)  TMA loads, per tile iteration, the V tile into a 3-stage
+//                      ring (8-column boxes, no swizzle: K-adjacent core
+//                      matrices 2 KB apart) and the P tile into a 4-stage ring
+//                      (two 64-column boxes, 128-byte swizzle); once per work
+//                      item the dO rows
 //                      (two buffers, so the next item's can land early); and
 //                      an L2 prefetch of the next P tile before it waits for
 //                      a free stage;
 //   MMA (1 lane)       tcgen05.mma dP tile = dO . V^T into one of two
-//                      tensor-memory accumulators, committed to mbarriers that
-//                      hand the accumulator to the epilogue and the V tile back
-//                      to the producer;
+//                      tensor-memory accumulators, as soon as the V tile has
+//                      landed, committed to mbarriers that hand the accumulator
+//                      to the epilogue and the V stage back to the producer;
 //   epilogue (16 warps) warp w reads lanes 32 (w % 4) .. + 31 (its rows) and
 //                      columns 32 (w / 4) .. + 31 of the accumulator, and forms
 //                      the row sums (pass 1) or writes dS over P in the stage
@@ -50,20 +51,21 @@ constexpr uint32_t kPrefetchAhead = 1;
 
 template <int D>
 struct AttnTma {
-    static constexpr int NS = D == 64 ? 3 : 2;                      // stages in the ring
+    static constexpr int NP = D == 64 ? 4 : 2;                      // stages of the P / dS ring
+    static constexpr int NV = D == 64 ? 3 : 2;                      // stages of the V ring
     static constexpr uint32_t op = kAttnRows * D * 2;               // 128 rows of dO or V
-    static constexpr uint32_t off_p = 0;                            // NS P / dS tiles (1024-aligned)
-    static constexpr uint32_t off_v = NS * kAttnPTileBytes;         // NS V tiles
-    static constexpr uint32_t off_do = off_v + NS * op;             // 2 dO tiles
+    static constexpr uint32_t off_p = 0;                            // NP P / dS tiles (1024-aligned)
+    static constexpr uint32_t off_v = NP * kAttnPTileBytes;         // NV V tiles
+    static constexpr uint32_t off_do = off_v + NV * op;             // 2 dO tiles
     static constexpr uint32_t off_red = off_do + 2 * op;            // 8 x 128 floats: row-sum exchange
     static constexpr uint32_t bytes = off_red + 8 * kAttnRows * 4 + 1024;   // + slack to align the base
     static constexpr uint32_t lbo = kAttnRows * 16;                 // K-adjacent core matrices (one 8-column box)
     static constexpr uint32_t sbo = 128;                            // row-adjacent core matrices
-    static constexpr uint32_t stage_tx = op + kAttnPTileBytes;      // bytes per tile iteration
 };
 
 struct AttnShared {
-    uint64_t full[3], empty[3], dsready[3];   // per stage
+    uint64_t pfull[4], pempty[4], dsready[4];   // per P stage
+    uint64_t vfull[3], vempty[3];               // per V stage
     uint64_t tfull[2], tempty[2];             // per accumulator
     uint64_t dofull[2], doempty[2];           // per dO buffer
     uint64_t red_in, red_out;                 // row-sum exchange between the column halves
@@ -125,7 +127,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
 {
     using IO = Pairs<T>;
     using TL = AttnTma<D>;
-    constexpr int NS = TL::NS;
+    constexpr int NP = TL::NP, NV = TL::NV;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ AttnShared sh;
 
@@ -136,10 +138,14 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
     uint8_t* smem = smem_raw + (base - raw_u32);
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            tc::mbar_init(&sh.full[s], 1);
-            tc::mbar_init(&sh.empty[s], 1 + kTmaEpiWarps);   // MMA commit + (16 epilogue warps or the store lane x 16)
+        for (int s = 0; s < NP; ++s) {
+            tc::mbar_init(&sh.pfull[s], 1);
+            tc::mbar_init(&sh.pempty[s], kTmaEpiWarps);   // 16 epilogue warps, or the store lane x 16
             tc::mbar_init(&sh.dsready[s], kTmaEpiWarps);
+        }
+        for (int s = 0; s < NV; ++s) {
+            tc::mbar_init(&sh.vfull[s], 1);
+            tc::mbar_init(&sh.vempty[s], 1);   // the MMA's commit
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&sh.tfull[a], 1);
@@ -162,7 +168,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
 
     if (warp == kWarpProducer) {
         if (lane == 0) {
-            uint32_t g = 0, itm = 0;
+            uint32_t g = 0, itm = 0, gv = 0, gp = 0;   // iterations; V and P loads issued
             bool ok = true;
             // A second cursor walks the same iterations kPrefetchAhead ahead of the
             // loads and prefetches the P tiles of pass 1 into L2, so that the TMA
@@ -194,7 +200,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 for (int kc = 0; kc < D / 8; ++kc)
                     tc::tma_load_3d(base + TL::off_do + p * TL::op + kc * TL::lbo, &tm_do, kc * 8, it.r0, z, &sh.dofull[p]);
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
-                    const uint32_t s = g % NS, ph = (g / NS) & 1u;
+                    const uint32_t sv = g % NV, phv = (g / NV) & 1u, sp = g % NP, php = (g / NP) & 1u;
                     const int32_t tc0 = (i < it.n_tiles ? i : i - it.n_tiles) * kAttnRows;
                     while (pf_live && pf_g <= g + kPrefetchAhead) {
                         if (pf_i < pf.n_tiles) {
@@ -210,26 +216,36 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                             pf_live = pf_seek();
                         }
                     }
-                    ok = tc::mbar_wait(&sh.empty[s], ph ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                    ok = tc::mbar_wait(&sh.vempty[sv], phv ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
                     if (!ok)
                         break;
-                    tc::mbar_arrive_expect_tx(&sh.full[s], TL::stage_tx);
+                    tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
                     for (int kc = 0; kc < D / 8; ++kc)
-                        tc::tma_load_3d(base + TL::off_v + s * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z, &sh.full[s]);
-                    const uint32_t pt = base + TL::off_p + s * kAttnPTileBytes;
+                        tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z, &sh.vfull[sv]);
+                    ++gv;
+                    ok = tc::mbar_wait(&sh.pempty[sp], php ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                    if (!ok)
+                        break;
+                    tc::mbar_arrive_expect_tx(&sh.pfull[sp], kAttnPTileBytes);
+                    ++gp;
+                    const uint32_t pt = base + TL::off_p + sp * kAttnPTileBytes;
                     // Pass 1 keeps the P tile in L2 for pass 2, which is its last read.
                     const uint64_t pol = i < it.n_tiles ? tc::policy_evict_last() : tc::policy_evict_first();
-                    tc::tma_load_3d(pt, &tm_p, tc0, it.r0, z, &sh.full[s], pol);
-                    tc::tma_load_3d(pt + kAttnRows * 128, &tm_p, tc0 + 64, it.r0, z, &sh.full[s], pol);
+                    tc::tma_load_3d(pt, &tm_p, tc0, it.r0, z, &sh.pfull[sp], pol);
+                    tc::tma_load_3d(pt + kAttnRows * 128, &tm_p, tc0 + 64, it.r0, z, &sh.pfull[sp], pol);
                 }
                 ++itm;
             }
             if (!ok) {
                 attn_abort(sh, status);
                 // Let the copies already issued land before the CTA can exit.
-                for (uint32_t k = 0; k < static_cast<uint32_t>(NS) && k < g; ++k) {
-                    const uint32_t gk = g - 1 - k;
-                    tc::mbar_wait(&sh.full[gk % NS], (gk / NS) & 1u, kAttnWaitLimit);
+                for (uint32_t k = 0; k < static_cast<uint32_t>(NV) && k < gv; ++k) {
+                    const uint32_t gk = gv - 1 - k;
+                    tc::mbar_wait(&sh.vfull[gk % NV], (gk / NV) & 1u, kAttnWaitLimit);
+                }
+                for (uint32_t k = 0; k < static_cast<uint32_t>(NP) && k < gp; ++k) {
+                    const uint32_t gk = gp - 1 - k;
+                    tc::mbar_wait(&sh.pfull[gk % NP], (gk / NP) & 1u, kAttnWaitLimit);
                 }
                 if (itm > 0)
                     tc::mbar_wait(&sh.dofull[(itm - 1) & 1u], ((itm - 1) >> 1) & 1u, kAttnWaitLimit);
@@ -250,19 +266,19 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                     break;
                 const uint32_t a_base = base + TL::off_do + p * TL::op;
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
-                    const uint32_t s = g % NS, ph = (g / NS) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
+                    const uint32_t sv = g % NV, phv = (g / NV) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
                     ok = tc::mbar_wait(&sh.tempty[acc], pha ^ 1u, kAttnWaitLimit) &&
-                         tc::mbar_wait(&sh.full[s], ph, kAttnWaitLimit) && !attn_aborted(sh);
+                         tc::mbar_wait(&sh.vfull[sv], phv, kAttnWaitLimit) && !attn_aborted(sh);
                     if (!ok)
                         break;
                     tc::fence_after_sync();
-                    const uint32_t b_base = base + TL::off_v + s * TL::op;
+                    const uint32_t b_base = base + TL::off_v + sv * TL::op;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
                         tc::mma_f16(tmem + acc * kAttnRows, tc::smem_desc(a_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo),
                                     tc::smem_desc(b_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo), idesc, ks > 0 ? 1u : 0u);
                     tc::commit(&sh.tfull[acc]);
-                    tc::commit(&sh.empty[s]);
+                    tc::commit(&sh.vempty[sv]);
                     issued = true;
                 }
                 if (!ok)
@@ -287,7 +303,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
                     if (i < it.n_tiles)
                         continue;
-                    const uint32_t s = g % NS;
+                    const uint32_t s = g % NP;
                     ok = tc::mbar_wait(&sh.dsready[s], (ds_par >> s) & 1u, kAttnWaitLimit) && !attn_aborted(sh);
                     if (!ok)
                         break;
@@ -300,7 +316,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                         tc::tma_store_3d(&tm_ds, tc0 + 64, it.r0, z, pt + kAttnRows * 128, pol);
                     tc::bulk_commit();
                     tc::bulk_wait_read_all();
-                    tc::mbar_arrive(&sh.empty[s], kTmaEpiWarps);
+                    tc::mbar_arrive(&sh.pempty[s], kTmaEpiWarps);
                 }
             }
             if (!ok)
@@ -340,7 +356,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 // Kept elements of this thread's 32 columns: the first `kept` of them.
                 const int32_t lim = live ? r - (tc0 + colq * 32) + 1 : 0;
                 const int kept = lim < 0 ? 0 : (lim > 32 ? 32 : lim);
-                const uint32_t s = g % NS, ph = (g / NS) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
+                const uint32_t s = g % NP, ph = (g / NP) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
                 ok = warp_wait(&sh.tfull[acc], pha) && !attn_aborted(sh);
                 if (!ok)
                     break;
@@ -351,7 +367,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive(&sh.tempty[acc]);
-                ok = warp_wait(&sh.full[s], ph);   // the P tile (landed before the MMA ran)
+                ok = warp_wait(&sh.pfull[s], ph);   // the P tile
                 if (!ok)
                     break;
                 uint8_t* p_row = smem + row_off + s * kAttnPTileBytes;
@@ -399,7 +415,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 if (!pass2) {
                     __syncwarp();
                     if (lane == 0)
-                        tc::mbar_arrive(&sh.empty[s]);
+                        tc::mbar_arrive(&sh.pempty[s]);
                     if (i == it.n_tiles - 1) {   // merge the four column quarters' row sums
                         const uint32_t rp = itm & 1u;
                         if (colq != 0) {
