@@ -75,20 +75,22 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-ATTN_SOURCES = ("gtms_attn_bwd.cu", "gtms_attn_bwd.cuh", "gtms_tcgen05.cuh", "gtms_kernels.cuh")
+def attention_source(name):
+    """Files the attention-backward kernels are compiled from (besides the shared gtms_kernels.cuh)."""
+    return name.startswith("gtms_attn") or name == "gtms_tcgen05.cuh"
 
 
 def kernel_source_sha(kernel=""):
     """Hash of the sources a kernel is compiled from: for the attention-backward
-    kernel its own files, for the softmax kernels every other file of csrc."""
+    kernels their own files, for the softmax kernels every other file of csrc;
+    gtms_kernels.cuh belongs to both."""
     import glob
 
     attn = kernel.startswith("gtms_attn")
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "masked_softmax_attention_gb300", "csrc", "*"))):
         name = os.path.basename(p)
-        wanted = name in ATTN_SOURCES if attn else (name == "gtms_kernels.cuh" or name not in ATTN_SOURCES)
-        if wanted:
+        if name == "gtms_kernels.cuh" or attention_source(name) == attn:
             with open(p, "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
