@@ -7,14 +7,13 @@
 //
 // One CTA per SM walks the (slice, 128-row block) work items (see attn_item
 // for their order). Its warps:
-//   producer (1 lane)  TMA loads, per tile iteration, the V tile into a 3-stage
-//                      ring (8-column boxes, no swizzle: K-adjacent core
-//                      matrices 2 KB apart) and the P tile into a 4-stage ring
-//                      (two 64-column boxes, 128-byte swizzle); once per work
-//                      item the dO rows
-//                      (two buffers, so the next item's can land early); and
-//                      an L2 prefetch of the next P tile before it waits for
-//                      a free stage;
+//   producer (1 lane)  TMA loads, per tile iteration, the V tile into a ring of
+//                      NV stages (8-column boxes, no swizzle: K-adjacent core
+//                      matrices 2 KB apart) and the P tile into a ring of NP
+//                      stages (two 64-column boxes, 128-byte swizzle); once per
+//                      work item the dO rows (two buffers, so the next item's
+//                      can land early); and an L2 prefetch of the next P tile
+//                      before it waits for a free stage;
 //   MMA (1 lane)       tcgen05.mma dP tile = dO . V^T into one of two
 //                      tensor-memory accumulators, as soon as the V tile has
 //                      landed, committed to mbarriers that hand the accumulator
@@ -51,8 +50,10 @@ constexpr uint32_t kPrefetchAhead = 1;
 
 template <int D>
 struct AttnTma {
-    static constexpr int NP = D == 64 ? 4 : 2;                      // stages of the P / dS ring
-    static constexpr int NV = D == 64 ? 3 : 2;                      // stages of the V ring
+    // Stages of the P / dS ring and of the V ring: 213 KB of shared memory in
+    // all for head dim 64, 197 KB for 128.
+    static constexpr int NP = D == 64 ? 4 : 2;
+    static constexpr int NV = D == 64 ? 3 : 2;
     static constexpr uint32_t op = kAttnRows * D * 2;               // 128 rows of dO or V
     static constexpr uint32_t off_p = 0;                            // NP P / dS tiles (1024-aligned)
     static constexpr uint32_t off_v = NP * kAttnPTileBytes;         // NV V tiles
@@ -66,9 +67,9 @@ struct AttnTma {
 struct AttnShared {
     uint64_t pfull[4], pempty[4], dsready[4];   // per P stage
     uint64_t vfull[3], vempty[3];               // per V stage
-    uint64_t tfull[2], tempty[2];             // per accumulator
-    uint64_t dofull[2], doempty[2];           // per dO buffer
-    uint64_t red_in, red_out;                 // row-sum exchange between the column halves
+    uint64_t tfull[2], tempty[2];               // per accumulator
+    uint64_t dofull[2], doempty[2];             // per dO buffer
+    uint64_t red_in, red_out;                   // row-sum exchange between the column quarters
     uint32_t tmem_slot;
     int abort_flag;
 };
