@@ -218,6 +218,40 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return r;
 }
 
+// Softmax statistics of a row over a CTA team in one shared-memory exchange.
+// Each warp has reduced, with shuffles, its extreme e_w (max, or min when the
+// scale is negative) and its sum s_w of 2^((x - e_w) c) over its kept
+// elements. The warps' pairs meet once in `smem` (2 * TW / 32 floats; callers
+// alternate two buffers per row). Lane l of every warp then takes pair l, and
+// two butterflies give the row's extreme E and sum S = sum_w s_w 2^((e_w - E) c)
+// (the same operations in every warp, so every thread gets the same E and S).
+// Returns this warp's output factor 2^((e_w - E) c) / S. A warp with no kept
+// element has s_w == 0 and takes no part (a NaN sum still propagates).
+template <int TW>
+__device__ __forceinline__ float team_softmax_factor(float e_w, float s_w, float c, bool use_max, float* smem)
+{
+    constexpr int NW = TW / 32;
+    const int l = threadIdx.x & 31;
+    if (l == 0) {
+        smem[threadIdx.x >> 5] = e_w;
+        smem[NW + (threadIdx.x >> 5)] = s_w;
+    }
+    __syncthreads();
+    const float e_l = l < NW ? smem[l] : 0.0f, s_l = l < NW ? smem[NW + l] : 0.0f;
+    const bool has = s_l != 0.0f;
+    float E = has ? e_l : (use_max ? -INFINITY : INFINITY);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float other = __shfl_xor_sync(0xffffffffu, E, o);
+        E = use_max ? fmaxf(E, other) : fminf(E, other);
+    }
+    float S = has ? __fmul_rn(s_l, ex2(__fmul_rn(__fsub_rn(e_l, E), c))) : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
+    return s_w != 0.0f ? __fmul_rn(ex2(__fmul_rn(__fsub_rn(e_w, E), c)), __frcp_rn(S)) : 0.0f;
+}
+
 __device__ __forceinline__ float min3(float a, float b, float c)
 {
     float r;
@@ -553,14 +587,19 @@ __device__ __forceinline__ void bwd_store(char* row, const Unit16 (&ry)[NV], con
 //
 // t = (x - x_ext) * (scale * log2 e) with x_ext the row max (scale >= 0) or min
 // (scale < 0): t <= 0 everywhere and exactly 0 at the extreme element, so a
-// one-element row gives exp = 1, sum = 1, y = 1.
+// one-element row gives exp = 1, sum = 1, y = 1. A 1024-thread team takes
+// x_ext per warp and rescales the warps' sums in its single shared-memory
+// exchange (team_softmax_factor); a one-element row still gives factor 1, y = 1.
 // ---------------------------------------------------------------------------
 template <typename T, int MK, int TW, int NV, int MINB>
 __global__ void __launch_bounds__(TW == 32 ? kWarpTeamBlock : TW, MINB)
 gtms_fwd_vec_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
     constexpr int EPU = 2 * Pairs<T>::kPairs;
-    __shared__ float red[TW > 32 ? 2 * (TW / 32) : 1];
+    // Two buffers of (extreme, sum) per warp, alternating per row (a fast warp
+    // could otherwise overwrite a slot a slow warp is still reading).
+    __shared__ float red[2][TW > 32 ? 2 * (TW / 32) : 1];
+    int par = 0;
 
     const float c = __fmul_rn(scale, kLog2e);
     const bool use_max = scale >= 0.0f;
@@ -585,9 +624,22 @@ gtms_fwd_vec_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom
 
         float2 v[NV][Pairs<T>::kPairs];
         float ext = fwd_decode_extreme<T, NV>(raw, v, ur, unit_of, use_max);
-        ext = use_max ? team_max<TW>(ext, red) : -team_max<TW>(-ext, red);
-        const float s = team_sum<TW>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), red + (TW > 32 ? TW / 32 : 0));
-        fwd_store<T, NV>(yr, v, ur, unit_of, __frcp_rn(s));
+        if constexpr (TW >= 1024) {
+            // exps relative to the warp's extreme; one exchange rescales the warps' sums
+            // (saves a CTA-wide round; measured on GB300 it pays only for 1024-thread
+            // teams, +9 % at S = 32768 bf16, and costs 2-5 % for teams of 64-256)
+            ext = use_max ? team_max<32>(ext, nullptr) : -team_max<32>(-ext, nullptr);
+            const float s_w = team_sum<32>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), nullptr);
+            const float f = team_softmax_factor<TW>(ext, s_w, c, use_max, red[par]);
+            par ^= 1;
+            fwd_store<T, NV>(yr, v, ur, unit_of, f);
+        } else {
+            float* red_max = red[0];
+            float* red_sum = TW > 32 ? red[0] + TW / 32 : red[0];
+            ext = use_max ? team_max<TW>(ext, red_max) : -team_max<TW>(-ext, red_max);
+            const float s = team_sum<TW>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), red_sum);
+            fwd_store<T, NV>(yr, v, ur, unit_of, __frcp_rn(s));
+        }
     }
 }
 
