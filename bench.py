@@ -248,10 +248,12 @@ def cpu_model():
             info = f.read()
     except OSError:
         return None
+    arm_parts = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd8e": "Arm Neoverse-N3"}
     for key in ("model name", "Model Name", "CPU part"):
         for line in info.splitlines():
             if line.startswith(key):
-                return line.split(":", 1)[1].strip()
+                v = line.split(":", 1)[1].strip()
+                return f"{arm_parts[v]} (CPU part {v})" if v in arm_parts else v
     return None
 
 
