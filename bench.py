@@ -403,16 +403,20 @@ def run_gpu_attention(args, w, lens, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     s_ev.record(stream)
     rc = 0
-    for _ in range(args.steps):
+    for a, b in ev:
+        a.record(stream)
         rc |= fn(*args_c)
+        b.record(stream)
     e_ev.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if rc or int(status.item()):
         raise RuntimeError("gtms_attention_softmax_backward failed or timed out inside the timed region")
     ms = max_over_ranks(s_ev.elapsed_time(e_ev) / args.steps, dist, dev)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     fb, _ = required_bytes(wr, lens_r)                    # kept P read + every dS written
     nbytes = fb + 2 * wr.B * wr.M * wr.S * wr.head_dim * wr.elem_bytes
     value = whole_job_gbs(sum_over_ranks(nbytes, dist, dev), ms)
@@ -435,6 +439,7 @@ def run_gpu_attention(args, w, lens, rank, world, local_rank):
             "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "ms_per_step_median": round(statistics.median(step_ms), 5), "ms_per_step_min": round(min(step_ms), 5),
             "config": {**workload_config(w, lens),
                        "step": "gtms_attention_softmax_backward (dP = dO V^T on tcgen05, fused softmax backward)"},
             "kernels": {"attention_softmax_backward": {"kernel": kname, "ms_per_call": round(ms, 5),
