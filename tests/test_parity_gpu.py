@@ -698,3 +698,33 @@ def test_attention_softmax_backward_full_size_sampled(dev):
                     ds[b, m].reshape(1, 1, S, S), f"full size slice ({b},{m})")
     del p, ds, dout, v
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("lens", [(0, 0), (-5, 3000)])
+def test_attention_softmax_backward_padded_and_clamped_lengths(dev, lens):
+    """All-padded batches give an all-zero dS; seq_lens outside [0, S] are clamped."""
+    B, M, S, d, dtype = 2, 2, 256, 64, "bf16"
+    clamped = tuple(min(max(v, 0), S) for v in lens)
+    w, p_bits, dout, v = _attn_case(dev, B, M, S, d, dtype, clamped, seed=95)
+    p_d = from_bits(p_bits, dtype, "cpu").view(B, M, S, S).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    raw_lens = torch.tensor(lens, dtype=torch.int32, device=dev)
+    ds = torch.full_like(p_d, float("nan"))
+    gtms.attention_softmax_backward(p_d, dout.to(dev), v.to(dev), raw_lens, w.scale, out=ds, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _attn_check(w, d, p_bits, dout, v, ds, f"lens {lens}")
+
+
+def test_attention_softmax_backward_long_rows(dev):
+    """S = 8192: 64 row blocks, up to 64 tiles per block and 128 tile iterations per work item."""
+    B, M, S, d, dtype = 1, 1, 8192, 64, "bf16"
+    w, p_bits, dout, v = _attn_case(dev, B, M, S, d, dtype, (6001,), seed=96)
+    p_d = from_bits(p_bits, dtype, "cpu").view(B, M, S, S).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ds = torch.full_like(p_d, float("nan"))
+    gtms.attention_softmax_backward(p_d, dout.to(dev), v.to(dev), torch.from_numpy(si.seq_lens(w)).to(dev),
+                                    w.scale, out=ds, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _attn_check(w, d, p_bits, dout, v, ds, "S=8192")
