@@ -234,6 +234,15 @@ def test_tensor_api_rejects_cpu_tensors(lib):
         gtms.forward(x, lens)
     with pytest.raises(ValueError):
         gtms.backward(x, x, lens)
+    p = torch.zeros(1, 1, 4, 4, dtype=torch.bfloat16)
+    dv = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gtms.attention_softmax_backward(p, dv, dv, lens)
+    # the host-resident forms want page-locked tensors: ordinary CPU tensors are refused
+    with pytest.raises(ValueError):
+        gtms.attention_softmax_backward_host(p, dv, dv, lens)
+    with pytest.raises(ValueError):
+        gtms.forward_host(x, lens)
 
 
 def test_missing_library_fails_loudly(tmp_path):
