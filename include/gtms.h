@@ -169,10 +169,16 @@ int gtms_backward_explicit(const void* y, const void* dy, void* dx, const uint8_
  * on the grouped-tril kept entries (c <= r < L), +0.0 elsewhere, with
  * dP[r,c] = sum_k dO[b,m,r,k] V[b,m,c,k] accumulated in fp32 and never
  * written to memory.
- *   p        device, [B,M,S,S] of `dtype` (the forward output), read-only;
- *            only 16-byte units holding a kept entry are loaded.
- *   dout, v  device, [B,M,S,head_dim] of `dtype`, read-only.
- *   ds       device, [B,M,S,S] of `dtype`, every element written; may equal p.
+ *   p        [B,M,S,S] of `dtype` (the forward output), read-only. Masked
+ *            entries are never used (NaN there does not reach ds); tiles
+ *            right of the diagonal and padded row blocks are not read.
+ *   dout, v  [B,M,S,head_dim] of `dtype`, read-only.
+ *   ds       [B,M,S,S] of `dtype`, every element written; may equal p.
+ * The four tensors are device-addressable: when all four are device memory
+ * the call runs a persistent TMA-fed kernel (one CTA per SM); otherwise
+ * (mapped page-locked host memory, see gtms_device_pointer_of_host) a kernel
+ * that copies with cp.async and reads P only in 16-byte units that hold a
+ * kept entry.
  *   seq_lens device int32[B]; scale finite.
  *   head_dim 64 or 128; dtype GTMS_BF16 or GTMS_F16; S a multiple of 8.
  *   status   NULL, or a device int32 the kernel ORs 1 into if one of its
