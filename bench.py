@@ -42,18 +42,60 @@ DEFAULT_WORKLOAD = "s1000_b12"
 # Byte model
 # ---------------------------------------------------------------------------
 
-def required_bytes(w, lens):
-    """(forward bytes, backward bytes) the method must move for one call each."""
+def kept_per_slice(w, L):
+    """Kept elements of one (b, m) slice of length L under the workload's mask family."""
+    S = w.S
+    L = min(max(int(L), 0), S)
+    if w.mask_kind == 1:                 # length mask: c < L on rows r < L
+        return L * L
+    if w.mask_kind == 2:                 # sliding causal window of width win: min(r + 1, win) on rows r < L
+        win = min(max(int(w.window), 1), S)
+        full = min(L, win)
+        return full * (full + 1) // 2 + (L - full) * win
+    return L * (L + 1) // 2              # grouped tril: c <= r < L
+
+
+def required_bytes(w, lens, kept_total=None):
+    """(forward bytes, backward bytes) the method must move for one call each: the kept
+    elements read (x; y and dy), every output element written, and for an explicit-mask
+    workload its uint8 [B, S, S] mask once (the heads share it; kept_total: the mask's
+    kept count over all heads)."""
     S, e = w.S, w.elem_bytes
-    live = 0
-    for L in lens:
-        L = min(max(int(L), 0), S)
-        live += L * (L + 1) // 2
-    live *= w.M
+    live = kept_total if kept_total is not None else w.M * sum(kept_per_slice(w, L) for L in lens)
     dense = w.B * w.M * S * S
-    fwd = e * (live + dense)
-    bwd = e * (2 * live + dense) if w.backward else 0
+    mask = w.B * S * S if w.keep_prob > 0 else 0
+    fwd = e * (live + dense) + mask
+    bwd = e * (2 * live + dense) + mask if w.backward else 0
     return fwd, bwd
+
+
+def entry_points(lib, w):
+    """The C calls of one step of workload w: fwd(x, y, lens, mask, stream) and
+    bwd(y, dy, dx, lens, mask, stream) (pointers as ints; mask used by explicit-mask
+    workloads only), with the names of the entry points."""
+    B, M, S, code, scale = w.B, w.M, w.S, w.dtype_code, float(w.scale)
+    if w.keep_prob > 0:
+        return (lambda x, y, lp, mp, sp: lib.gtms_forward_explicit(x, y, mp, B, B, M, S, scale, code, sp),
+                lambda y, g, d, lp, mp, sp: lib.gtms_backward_explicit(y, g, d, mp, B, B, M, S, scale, code, sp),
+                "gtms_forward_explicit", "gtms_backward_explicit")
+    if w.mask_kind:
+        k, win = w.mask_kind, w.window
+        return (lambda x, y, lp, mp, sp: lib.gtms_forward_masked(x, y, lp, B, M, S, scale, k, win, code, sp),
+                lambda y, g, d, lp, mp, sp: lib.gtms_backward_masked(y, g, d, lp, B, M, S, scale, k, win, code, sp),
+                "gtms_forward_masked", "gtms_backward_masked")
+    return (lambda x, y, lp, mp, sp: lib.gtms_forward(x, y, lp, B, M, S, scale, code, sp),
+            lambda y, g, d, lp, mp, sp: lib.gtms_backward(y, g, d, lp, B, M, S, scale, code, sp),
+            "gtms_forward", "gtms_backward")
+
+
+def kernel_label(gtms, w, direction):
+    """Name of the kernel a call of workload w launches (same variant table for every mask)."""
+    name = gtms.kernel_name(direction, w.S, w.dtype_code, True)
+    if w.keep_prob > 0:
+        return name.replace("_vec_kernel", "_explicit_kernel")
+    if w.mask_kind:
+        return name.replace(">", f",mask{w.mask_kind}>")
+    return name
 
 
 # ---------------------------------------------------------------------------
@@ -189,7 +231,8 @@ def oracle_sample(w, lens, slices, device="cpu"):
     picked = [b for b, _ in slices]
     ws = si.Workload(w.name + "_sample", len(picked), 1, w.S, w.dtype, w.scale, x_std=w.x_std,
                      fixed_seq_lens=tuple(int(lens[b]) for b in picked), spike_prob=w.spike_prob,
-                     spike_value=w.spike_value, backward=w.backward, seed=w.seed + 7, head_dim=w.head_dim)
+                     spike_value=w.spike_value, backward=w.backward, seed=w.seed + 7, head_dim=w.head_dim,
+                     mask_kind=w.mask_kind, window=w.window, keep_prob=w.keep_prob)
     bits_t = {"f32": (np.uint32, "int32"), "bf16": (np.uint16, "int16"), "f16": (np.uint16, "int16")}[w.dtype]
     import torch
 
@@ -208,13 +251,21 @@ def oracle_sample(w, lens, slices, device="cpu"):
                                             threads=os.cpu_count() or 1), ws.dtype_code)
         dout, v = si.make_head_operands(ws, device)
         return ws, pb, (bits(dout), bits(v))
+    if ws.keep_prob > 0:   # explicit-mask sample: dy and the sample's own seeded keep mask
+        return ws, xb, (bits(si.make_dy(ws, device)), si.make_keep_mask(ws, device).numpy())
     return ws, xb, bits(si.make_dy(ws, device))
 
 
-def step_bytes(w, lens):
+def sample_bytes(ws, dyb):
+    """Algorithmic bytes of one oracle step over a sample from oracle_sample."""
+    kept = int((dyb[1] != 0).sum()) * ws.M if ws.keep_prob > 0 else None
+    return step_bytes(ws, ws.fixed_seq_lens, kept)
+
+
+def step_bytes(w, lens, kept_total=None):
     """Algorithmic bytes of one step: the softmax forward + backward, or for an
     attention-backward workload the kept P read, every dS written, dO and V read."""
-    fb, bb = required_bytes(w, lens)
+    fb, bb = required_bytes(w, lens, kept_total)
     if w.head_dim > 0:
         return fb + 2 * w.B * w.M * w.S * w.head_dim * w.elem_bytes
     return fb + bb
@@ -234,10 +285,19 @@ def oracle_step(ws, xb, dyb, threads):
                                  threads=threads)
         oracle.round_to(ds, ws.dtype_code)
         return
-    y = oracle.forward(xb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
+    if ws.keep_prob > 0:
+        dyb, mask = dyb
+        y = oracle.forward_explicit(xb, mask, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
+        yb = oracle.round_to(y, ws.dtype_code)
+        if ws.backward:
+            dx = oracle.backward_explicit(yb, dyb, mask, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
+            oracle.round_to(dx, ws.dtype_code)
+        return
+    kw = dict(threads=threads, mask_kind=ws.mask_kind, window=ws.window)
+    y = oracle.forward(xb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, **kw)
     yb = oracle.round_to(y, ws.dtype_code)
     if ws.backward:
-        dx = oracle.backward(yb, dyb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
+        dx = oracle.backward(yb, dyb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, **kw)
         oracle.round_to(dx, ws.dtype_code)
 
 
@@ -270,13 +330,13 @@ def cpu_baseline(w, lens, budget_s=12.0):
         t0 = time.perf_counter()
         oracle_step(ws, xb, dyb, threads)
         total_s += time.perf_counter() - t0
-        total_bytes += step_bytes(ws, ws.fixed_seq_lens)
+        total_bytes += sample_bytes(ws, dyb)
         done_slices += group
         groups += 1
     ws, xb, dyb = oracle_sample(w, lens, [(b % w.B, 0) for b in range(min(4, w.B * w.M))])
     t0 = time.perf_counter()
     oracle_step(ws, xb, dyb, 1)
-    single = step_bytes(ws, ws.fixed_seq_lens) / (time.perf_counter() - t0) / 1e9
+    single = sample_bytes(ws, dyb) / (time.perf_counter() - t0) / 1e9
     return {"value": round(total_bytes / total_s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "value_1_thread": round(single, 4), "cpu_model": cpu_model(),
             "sample": f"{done_slices} (b,m) slices of {w.name} (S={w.S}, the workload's seq_lens and value "
@@ -286,6 +346,17 @@ def cpu_baseline(w, lens, budget_s=12.0):
 
 def oracle_step_name(w):
     return "oracle dS step from (P, dO, V) + round" if w.head_dim > 0 else "oracle forward + round + backward"
+
+
+def full_kept_total(w):
+    """Kept entries of the whole workload's explicit keep mask, over all heads (None for mask families)."""
+    if w.keep_prob <= 0:
+        return None
+    import torch
+
+    import seeded_inputs as si
+
+    return int(torch.count_nonzero(si.make_keep_mask(w, "cpu")).item()) * w.M
 
 
 def run_reference(args, w, lens):
@@ -300,13 +371,13 @@ def run_reference(args, w, lens):
     for _ in range(args.steps):
         oracle_step(ws, xb, dyb, threads)
     dt = (time.perf_counter() - t0) / max(1, args.steps)
-    value = step_bytes(ws, ws.fixed_seq_lens) / dt / 1e9
+    value = sample_bytes(ws, dyb) / dt / 1e9
     sample = (f"1 (b,m) slice of {w.name} per step (S={w.S}, seq_len={ws.fixed_seq_lens[0]}, drawn on the "
               f"CPU): {oracle_step_name(w)}")
     line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-            "data": "synthetic", "config": workload_config(w, lens),
+            "data": "synthetic", "config": workload_config(w, lens, full_kept_total(w)),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -356,8 +427,8 @@ def whole_job_gbs(total_bytes, ms_step):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def workload_config(w, lens):
-    fb, bb = required_bytes(w, lens)
+def workload_config(w, lens, kept_total=None):
+    fb, bb = required_bytes(w, lens, kept_total)
     return {"workload": w.name + ": " + w.describe(), "B": w.B, "M": w.M, "S": w.S, "dtype": w.dtype,
             "scale": w.scale, "seq_lens_seeded": [int(v) for v in lens] if len(lens) <= 16 else "see seed",
             "seed": w.seed, **({"head_dim": w.head_dim, "required_bytes_step": step_bytes(w, lens)}
@@ -527,18 +598,21 @@ def run_gpu(args, w, lens, rank, world, local_rank):
     lens_d = torch.from_numpy(lens_r).to(dev)
     y = torch.empty_like(x)
     dx = torch.empty_like(x)
-    B, M, S, code, scale = wr.B, wr.M, wr.S, wr.dtype_code, float(wr.scale)
+    S, code = wr.S, wr.dtype_code
+    mask = si.make_keep_mask(wr, dev) if wr.keep_prob > 0 else None
+    kept_total = int(torch.count_nonzero(mask).item()) * wr.M if mask is not None else None
     xp, yp, dyp, dxp, lp = x.data_ptr(), y.data_ptr(), dy.data_ptr(), dx.data_ptr(), lens_d.data_ptr()
-    fwd_c, bwd_c = gtms.load_library().gtms_forward, gtms.load_library().gtms_backward
+    mp = mask.data_ptr() if mask is not None else None
+    fwd_c, bwd_c, fwd_name, bwd_name = entry_points(gtms.load_library(), wr)
 
     def step():
-        rc = fwd_c(xp, yp, lp, B, M, S, scale, code, sp)
+        rc = fwd_c(xp, yp, lp, mp, sp)
         if rc:
-            raise gtms.GtmsError("gtms_forward", rc)
+            raise gtms.GtmsError(fwd_name, rc)
         if wr.backward:
-            rc = bwd_c(yp, dyp, dxp, lp, B, M, S, scale, code, sp)
+            rc = bwd_c(yp, dyp, dxp, lp, mp, sp)
             if rc:
-                raise gtms.GtmsError("gtms_backward", rc)
+                raise gtms.GtmsError(bwd_name, rc)
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     for _ in range(args.warmup):
@@ -555,10 +629,10 @@ def run_gpu(args, w, lens, rank, world, local_rank):
     start.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
-        rc = fwd_c(xp, yp, lp, B, M, S, scale, code, sp)
+        rc = fwd_c(xp, yp, lp, mp, sp)
         ev[k][1].record(stream)
         if wr.backward:
-            rc |= bwd_c(yp, dyp, dxp, lp, B, M, S, scale, code, sp)
+            rc |= bwd_c(yp, dyp, dxp, lp, mp, sp)
         ev[k][2].record(stream)
         if rc:
             raise RuntimeError("libgtms call failed inside the timed region")
@@ -574,7 +648,7 @@ def run_gpu(args, w, lens, rank, world, local_rank):
     ms_step = max_over_ranks(total_ms / K, dist, dev)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
 
-    fb, bb = required_bytes(wr, lens_r)
+    fb, bb = required_bytes(wr, lens_r, kept_total)
     value = whole_job_gbs(sum_over_ranks(fb + bb, dist, dev), ms_step)
 
     peak, peak_kind = hbm_peak()
@@ -582,7 +656,7 @@ def run_gpu(args, w, lens, rank, world, local_rank):
     for name, nbytes, ms, direction in (("forward", fb, fwd_ms, 0), ("backward", bb, bwd_ms, 1)):
         if nbytes == 0:
             continue
-        kname = gtms.kernel_name(direction, S, code, True)
+        kname = kernel_label(gtms, wr, direction)
         gbs = nbytes / (ms * 1e-3) / 1e9
         kern[name] = {"kernel": kname, "ms_per_call": round(ms, 5), "required_bytes": nbytes,
                       "achieved_gbs": round(gbs, 2), "frac_of_peak": round(gbs / peak, 4)}
@@ -596,8 +670,9 @@ def run_gpu(args, w, lens, rank, world, local_rank):
 
     e2e = e2e_staged = None
     if args.e2e_steps > 0:
-        e2e = run_e2e_host_resident(args, wr, lens_r, dev, stream, fwd_c, bwd_c)
-        e2e_staged = run_e2e(args, wr, lens_r, dev, stream, fwd_c, bwd_c)
+        e2e = run_e2e_host_resident(args, wr, lens_r, dev, stream, fwd_c, bwd_c, mask, kept_total)
+        if mask is None and not wr.mask_kind:   # the staged pipeline serves the default op
+            e2e_staged = run_e2e(args, wr, lens_r, dev, stream)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, lens)
@@ -608,7 +683,7 @@ def run_gpu(args, w, lens, rank, world, local_rank):
         line = {"metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-                "config": workload_config(w, lens), "pct_hbm_peak": round(100 * (value / world) / peak, 2),
+                "config": workload_config(wr, lens_r, kept_total), "pct_hbm_peak": round(100 * (value / world) / peak, 2),
                 "ms_per_step_median": round(statistics.median(step_ms), 5), "ms_per_step_min": round(min(step_ms), 5),
                 "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_staged": e2e_staged,
                 "gpu_launches": K * (2 if wr.backward else 1), "clocks": clocks,
@@ -618,10 +693,11 @@ def run_gpu(args, w, lens, rank, world, local_rank):
         dist.destroy_process_group()
 
 
-def run_e2e_host_resident(args, w, lens, dev, stream, fwd_c, bwd_c):
+def run_e2e_host_resident(args, w, lens, dev, stream, fwd_c, bwd_c, mask=None, kept_total=None):
     """The step through the C ABI with every tensor in pinned host memory: the
     kernels read the kept inputs from, and write every output to, host memory
-    over the host link (gtms_device_pointer_of_host), no staging copy."""
+    over the host link (gtms_device_pointer_of_host), no staging copy. An
+    explicit keep mask (`mask`, on the device) is copied to pinned memory too."""
     import torch
 
     import masked_softmax_attention_gb300 as gtms
@@ -638,18 +714,20 @@ def run_e2e_host_resident(args, w, lens, dev, stream, fwd_c, bwd_c):
     if w.backward:
         dy_h.copy_(si.make_dy(w, dev))
     lens_h = torch.from_numpy(lens).pin_memory()
+    mask_h = mask.cpu().pin_memory() if mask is not None else None
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     dp = gtms.device_pointer_of_host
     xp, yp, lp = dp(x_h.data_ptr()), dp(y_h.data_ptr()), dp(lens_h.data_ptr())
     dyp = dp(dy_h.data_ptr()) if w.backward else None
     dxp = dp(dx_h.data_ptr()) if w.backward else None
-    B, M, S, code, scale, sp = w.B, w.M, w.S, w.dtype_code, float(w.scale), stream.cuda_stream
+    mp = dp(mask_h.data_ptr()) if mask_h is not None else None
+    sp = stream.cuda_stream
 
     def step():
-        rc = fwd_c(xp, yp, lp, B, M, S, scale, code, sp)
+        rc = fwd_c(xp, yp, lp, mp, sp)
         if w.backward:
-            rc |= bwd_c(yp, dyp, dxp, lp, B, M, S, scale, code, sp)
+            rc |= bwd_c(yp, dyp, dxp, lp, mp, sp)
         if rc:
             raise RuntimeError("libgtms call failed in the end-to-end loop")
 
@@ -662,10 +740,11 @@ def run_e2e_host_resident(args, w, lens, dev, stream, fwd_c, bwd_c):
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / args.e2e_steps
-    fb, bb = required_bytes(w, lens)
+    fb, bb = required_bytes(w, lens, kept_total)
     dense = w.B * w.M * w.S * w.S * w.elem_bytes
-    kept = fb - dense                       # kept-prefix bytes of one tensor
-    h2d = kept + (2 * kept if w.backward else 0) + 4 * w.B
+    mask_reads = w.B * w.M * w.S * w.S if mask is not None else 0   # each row reads its mask row over the link
+    kept = fb - dense - (w.B * w.S * w.S if mask is not None else 0)   # kept bytes of one tensor
+    h2d = kept + (2 * kept if w.backward else 0) + 4 * w.B + mask_reads * (2 if w.backward else 1)
     d2h = dense * (2 if w.backward else 1)
     return {"value": round((fb + bb) / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
@@ -673,7 +752,7 @@ def run_e2e_host_resident(args, w, lens, dev, stream, fwd_c, bwd_c):
                             "over NVLink-C2C (no staging copy)"}
 
 
-def run_e2e(args, w, lens, dev, stream, fwd_c, bwd_c):
+def run_e2e(args, w, lens, dev, stream):
     """Same step through the public host-buffer API: inputs in pinned host
     memory, H2D of x, dy, seq_lens and D2H of y, dx inside the timed region
     (chunks of batches pipelined over three streams)."""

@@ -4,10 +4,11 @@
 //
 // The mask is uint8 [mask_batches, S, S] (mask_batches 1 or B), shared by the M
 // heads; a nonzero byte keeps the entry. Kept entries of a row need not be
-// contiguous, so every unit is masked per element. Each thread first loads the
-// mask bytes of its 16-byte units (4 bytes per fp32 unit, 8 per 16-bit unit);
-// a unit with no kept element loads no x and is stored as +0.0, so masked
-// inputs are still never read. The arithmetic is the vector kernels' (fp32
+// contiguous, so every unit is masked per element. A team takes one (batch,
+// row) pair and its M heads: each thread loads the mask bytes of its 16-byte
+// units once (4 bytes per fp32 unit, 8 per 16-bit unit) and keeps the bits
+// for every head; a unit with no kept element loads no x and is stored as
+// +0.0, so masked inputs are still never read. The arithmetic is the vector kernels' (fp32
 // pairs, one ex2.approx.f32 per kept element, float-float backward dot).
 #pragma once
 
@@ -60,19 +61,22 @@ gtms_fwd_explicit_kernel(const T* x, T* y, const uint8_t* __restrict__ mask, int
     int64_t team, nteams;
     team_coords<TW>(tid, team, nteams);
 
-    for (int64_t q = team; q < g.rows; q += nteams) {
-        int32_t b, r;
-        g.locate(q, b, r);
+    // A team takes one (batch, row) pair and all M heads of it: the row's mask
+    // bits are read once and serve every head.
+    const int32_t M = static_cast<int32_t>(g.rows_per_b / g.S);
+    for (int64_t qm = team; qm < g.rows / M; qm += nteams) {
+        const int32_t b = static_cast<int32_t>(qm / g.S), r = static_cast<int32_t>(qm % g.S);
         const uint8_t* mrow = explicit_mask_row(mask, mask_batches, b, r, g.S);
-        const char* xr = reinterpret_cast<const char*>(x + q * g.S);
-        char* yr = reinterpret_cast<char*>(y + q * g.S);
-
         uint32_t kb[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
             kb[k] = j < g.units ? keep_bits<EPU>(mrow, j) : 0u;
         }
+      for (int32_t m = 0; m < M; ++m) {
+        const int64_t q = (static_cast<int64_t>(b) * M + m) * g.S + r;
+        const char* xr = reinterpret_cast<const char*>(x + q * g.S);
+        char* yr = reinterpret_cast<char*>(y + q * g.S);
         Unit16 raw[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -129,6 +133,7 @@ gtms_fwd_explicit_kernel(const T* x, T* y, const uint8_t* __restrict__ mask, int
                 store16(yr + 16 * j, o);
             }
         }
+      }
     }
 }
 
@@ -146,20 +151,22 @@ gtms_bwd_explicit_kernel(const T* y, const T* dy, T* dx, const uint8_t* __restri
     team_coords<TW>(tid, team, nteams);
     const float2 sc = splat2(scale);
 
-    for (int64_t q = team; q < g.rows; q += nteams) {
-        int32_t b, r;
-        g.locate(q, b, r);
+    // A team takes one (batch, row) pair and all M heads of it (mask bits read once).
+    const int32_t M = static_cast<int32_t>(g.rows_per_b / g.S);
+    for (int64_t qm = team; qm < g.rows / M; qm += nteams) {
+        const int32_t b = static_cast<int32_t>(qm / g.S), r = static_cast<int32_t>(qm % g.S);
         const uint8_t* mrow = explicit_mask_row(mask, mask_batches, b, r, g.S);
-        const char* yr = reinterpret_cast<const char*>(y + q * g.S);
-        const char* gr = reinterpret_cast<const char*>(dy + q * g.S);
-        char* dr = reinterpret_cast<char*>(dx + q * g.S);
-
         uint32_t kb[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
             kb[k] = j < g.units ? keep_bits<EPU>(mrow, j) : 0u;
         }
+      for (int32_t m = 0; m < M; ++m) {
+        const int64_t q = (static_cast<int64_t>(b) * M + m) * g.S + r;
+        const char* yr = reinterpret_cast<const char*>(y + q * g.S);
+        const char* gr = reinterpret_cast<const char*>(dy + q * g.S);
+        char* dr = reinterpret_cast<char*>(dx + q * g.S);
         Unit16 ry[NV], rg[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -218,6 +225,7 @@ gtms_bwd_explicit_kernel(const T* y, const T* dy, T* dx, const uint8_t* __restri
                 store16(dr + 16 * j, o);
             }
         }
+      }
     }
 }
 
@@ -236,7 +244,7 @@ void launch_forward_explicit(int id, const void* x, void* y, const uint8_t* mask
     const T* xp = static_cast<const T*>(x);
     T* yp = static_cast<T*>(y);
 #define GTMS_EX_FWD_CASE(vid, tw, nv, mb) \
-    case vid: gtms_fwd_explicit_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, mask, mask_batches, g, scale); break;
+    case vid: gtms_fwd_explicit_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows / (g.rows_per_b / g.S)), block_for<tw>(), 0, st>>>(xp, yp, mask, mask_batches, g, scale); break;
     if constexpr (sizeof(T) == 4) {
         switch (id) { GTMS_FWD_VEC4(GTMS_EX_FWD_CASE) default: break; }
     } else {
@@ -253,7 +261,7 @@ void launch_backward_explicit(int id, const void* y, const void* dy, void* dx, c
     const T* gp = static_cast<const T*>(dy);
     T* dp = static_cast<T*>(dx);
 #define GTMS_EX_BWD_CASE(vid, tw, nv, mb) \
-    case vid: gtms_bwd_explicit_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, mask, mask_batches, g, scale); break;
+    case vid: gtms_bwd_explicit_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows / (g.rows_per_b / g.S)), block_for<tw>(), 0, st>>>(yp, gp, dp, mask, mask_batches, g, scale); break;
     if constexpr (sizeof(T) == 4) {
         switch (id) { GTMS_BWD_VEC4(GTMS_EX_BWD_CASE) default: break; }
     } else {

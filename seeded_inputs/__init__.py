@@ -30,6 +30,10 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
 * ``attn_s2048_bf16`` -- the attention-backward step at the ``s2048_bf16``
   shape: P the softmax of X[32,16,2048,2048] (bf16, variance 4,
   seq_len ~ U{1024..2048}, scale 0.125), dO and V [32,16,2048,64] ~ N(0,1).
+* ``length_s2048_bf16``, ``window_s2048_bf16``, ``explicit_s2048_bf16`` -- the
+  ``s2048_bf16`` shape and distribution under the length mask, a sliding causal
+  window of width 256, and an explicit uint8 keep mask (``make_keep_mask``:
+  each c <= r < seq_len entry kept with probability 1/2).
 * ``attn_s2048_b4`` -- ``attn_s2048_bf16`` with 4 batches: a profiler stand-in
   (P and dS 537 MB each, still larger than L2).
 * ``s1000_b2`` -- X[2,64,1000,1000], otherwise like ``s1000_b12``: a small
@@ -67,6 +71,9 @@ class Workload:
     backward: bool = True
     seed: int = 20261202
     head_dim: int = 0                       # > 0: attention-backward step workload (dO, V of this width)
+    mask_kind: int = 0                      # 0 grouped tril, 1 length mask, 2 sliding causal window
+    window: int = 0                         # band width for mask_kind 2
+    keep_prob: float = 0.0                  # > 0: explicit uint8 keep mask (see make_keep_mask)
 
     @property
     def rows(self) -> int:
@@ -99,6 +106,12 @@ class Workload:
         if self.head_dim > 0:
             return (f"dS from P=softmax(X[{self.B},{self.M},{self.S},{self.S}] {self.dtype} {dist} {lens} "
                     f"scale={self.scale:g}), dO and V [{self.B},{self.M},{self.S},{self.head_dim}] N(0,1)")
+        if self.keep_prob > 0:
+            lens += f", explicit uint8 keep mask [B,S,S]: c<=r<L kept with p={self.keep_prob:g}"
+        elif self.mask_kind == 1:
+            lens += ", length mask (c<L, r<L)"
+        elif self.mask_kind == 2:
+            lens += f", sliding causal window w={self.window}"
         return (f"X[{self.B},{self.M},{self.S},{self.S}] {self.dtype} {dist} {lens} scale={self.scale:g} "
                 f"{'fwd+bwd' if self.backward else 'fwd'}")
 
@@ -124,6 +137,13 @@ WORKLOADS = {
     # attention-backward step (dS from P, dO, V) at the bf16 S = 2048 shape, head_dim 64
     "attn_s2048_bf16": Workload("attn_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
                                 seq_len_range=(1024, 2048), seed=20261212, head_dim=64),
+    # the other mask families and an explicit keep mask, on the s2048_bf16 shape and distribution
+    "length_s2048_bf16": Workload("length_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
+                                  seq_len_range=(1024, 2048), seed=20261214, mask_kind=1),
+    "window_s2048_bf16": Workload("window_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
+                                  seq_len_range=(1024, 2048), seed=20261215, mask_kind=2, window=256),
+    "explicit_s2048_bf16": Workload("explicit_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
+                                    seq_len_range=(1024, 2048), seed=20261216, keep_prob=0.5),
     # profiling stand-in for attn_s2048_bf16: same distribution, 4 of the 32 batches
     "attn_s2048_b4": Workload("attn_s2048_b4", 4, 16, 2048, "bf16", 0.125, x_std=2.0,
                               seq_len_range=(1024, 2048), seed=20261212, head_dim=64),
@@ -187,6 +207,22 @@ def make_x(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.T
 def make_dy(w: Workload, device="cpu", max_chunk_elems: int = 1 << 28) -> torch.Tensor:
     """Upstream gradient dY[B,M,S,S] ~ N(0,1) in the workload's dtype."""
     return _draw(w, device, 1, 1.0, False, max_chunk_elems)
+
+
+def make_keep_mask(w: Workload, device="cpu") -> torch.Tensor:
+    """uint8 [B, S, S] explicit keep mask: entry (b, r, c) is 1 with probability keep_prob
+    where c <= r < seq_len[b], else 0 (independent seeded draws, one batch at a time)."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(w.seed * 4 + 7)
+    lens = seq_lens(w)
+    r = torch.arange(w.S, device=dev)
+    causal = r[None, :] <= r[:, None]
+    out = torch.empty(w.B, w.S, w.S, dtype=torch.uint8, device=dev)
+    for b in range(w.B):
+        u = torch.rand(w.S, w.S, generator=g, device=dev)
+        live = causal & (r[:, None] < int(lens[b]))
+        out[b] = (live & (u < w.keep_prob)).to(torch.uint8)
+    return out
 
 
 def make_head_operands(w: Workload, device="cpu"):
