@@ -43,8 +43,8 @@
  *                        not aligned to its element size, partial overlap.
  *   GTMS_ERR_UNSUPPORTED unknown dtype; S > GTMS_MAX_S; or S > 8192 with a row
  *                        whose byte length is not a multiple of 16 or a buffer
- *                        that is not 16-byte aligned (long rows are split over a
- *                        cluster of CTAs in 16-byte units only).
+ *                        that is not 16-byte aligned (long rows are streamed
+ *                        in 16-byte units only).
  *   GTMS_ERR_CUDA        the kernel launch failed (cudaGetLastError()).
  * All argument checks run on the host before anything is enqueued; a call
  * that returns an error has enqueued nothing.

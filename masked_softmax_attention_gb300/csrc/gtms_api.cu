@@ -305,7 +305,7 @@ GTMS_EXPORT int gtms_forward_explicit(const void* x, void* y, const uint8_t* mas
     const int ce = check_explicit(c, B, S, e, mask, mask_batches, y, aligned_to(x, 16) && aligned_to(y, 16));
     if (ce != GTMS_OK)
         return ce;
-    const int variant = gtms::pick_variant(0, S, e, true);
+    const int variant = gtms::pick_variant(0, S, e, true, false);
     const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e, 0);
     const int32_t mb = static_cast<int32_t>(mask_batches);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -332,7 +332,7 @@ GTMS_EXPORT int gtms_backward_explicit(const void* y, const void* dy, void* dx, 
     const int ce = check_explicit(c, B, S, e, mask, mask_batches, dx, a16);
     if (ce != GTMS_OK)
         return ce;
-    const int variant = gtms::pick_variant(1, S, e, true);
+    const int variant = gtms::pick_variant(1, S, e, true, false);
     const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e, 0);
     const int32_t mb = static_cast<int32_t>(mask_batches);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -432,7 +432,7 @@ GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, in
 {
     static const char* const kDtype[3] = {"f32", "bf16", "f16"};
     constexpr int kMaxRows = 16;
-    // [direction][dtype][vector rows, element rows, cluster rows], filled once (thread-safe static init).
+    // [direction][dtype][vector, element, stream rows], filled once (thread-safe static init).
     struct Names {
         char text[2][3][3 * kMaxRows][80];
         Names()
@@ -449,12 +449,11 @@ GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, in
                         std::snprintf(text[d][t][kMaxRows + i], sizeof text[d][t][kMaxRows + i],
                                       "gtms_%s_elem_kernel<%s,team%d,x%d>", d == 0 ? "fwd" : "bwd", kDtype[t],
                                       gtms::kElem[i].team, gtms::kElem[i].per_thread);
-                    const gtms::VariantTable ct = gtms::cluster_table(d, e);
-                    for (int i = 0; i < ct.count && i < kMaxRows; ++i)
+                    const gtms::VariantTable st = gtms::stream_table(d, e);
+                    for (int i = 0; i < st.count && i < kMaxRows; ++i)
                         std::snprintf(text[d][t][2 * kMaxRows + i], sizeof text[d][t][2 * kMaxRows + i],
-                                      "gtms_%s_cluster_kernel<%s,cluster%d,team%d,x%d,minb%d>", d == 0 ? "fwd" : "bwd",
-                                      kDtype[t], ct.rows[i].cluster, ct.rows[i].team, ct.rows[i].per_thread,
-                                      ct.rows[i].min_ctas);
+                                      "gtms_%s_stream_kernel<%s,team%d,x%d,minb%d>", d == 0 ? "fwd" : "bwd", kDtype[t],
+                                      st.rows[i].team, st.rows[i].per_thread, st.rows[i].min_ctas);
                 }
         }
     };
@@ -465,8 +464,8 @@ GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, in
     const int v = gtms::pick_variant(direction, S, e, aligned16 != 0);
     if (v < 0)
         return "none";
-    if (v >= gtms::kClusterBase)
-        return names.text[direction][dtype][2 * kMaxRows + v - gtms::kClusterBase];
+    if (v >= gtms::kStreamBase)
+        return names.text[direction][dtype][2 * kMaxRows + v - gtms::kStreamBase];
     return v >= gtms::kElemBase ? names.text[direction][dtype][kMaxRows + v - gtms::kElemBase]
                                 : names.text[direction][dtype][v];
 }

@@ -1,8 +1,8 @@
 // gtms_kernels.cuh -- sm_103a kernels of the grouped-tril masked softmax.
 //
 // One "team" of threads owns one row of X[B,M,S,S] at a time: a warp for short
-// rows, a whole CTA for long ones (rows longer than one CTA holds go to the
-// cluster kernels of gtms_cluster.cuh). The kept set of row r in batch b is a
+// rows, a whole CTA for long ones (rows of 32 KB and more go to the two-pass
+// stream kernels of gtms_stream.cuh). The kept set of row r in batch b is a
 // contiguous column range [c0, c1) computed from (r, L_b, mask kind), with
 // L_b = clamp(seq_lens[b], 0, S). For the default op ("Attention-Mask-
 // Optimization" README, operator behaviour: kept iff r < L, c < L and c <= r)
@@ -386,9 +386,9 @@ struct UnitRange {
 };
 
 // ---------------------------------------------------------------------------
-// Row stages shared by the per-row vector kernels and the cluster kernels. A
+// Row stages shared by the per-row vector kernels and the stream kernels. A
 // thread holds NV slots; unit_of(k) is the row unit of slot k (row units are
-// 16 bytes; UnitOf differs only in how slots interleave across the team).
+// 16 bytes; UnitOf differs only in which units a thread's slots cover).
 // ---------------------------------------------------------------------------
 
 // Loads of the kept units only.
@@ -587,19 +587,19 @@ __device__ __forceinline__ void bwd_store(char* row, const Unit16 (&ry)[NV], con
 //
 // t = (x - x_ext) * (scale * log2 e) with x_ext the row max (scale >= 0) or min
 // (scale < 0): t <= 0 everywhere and exactly 0 at the extreme element, so a
-// one-element row gives exp = 1, sum = 1, y = 1. A 1024-thread team takes
-// x_ext per warp and rescales the warps' sums in its single shared-memory
-// exchange (team_softmax_factor); a one-element row still gives factor 1, y = 1.
+// one-element row gives exp = 1, sum = 1, y = 1.
 // ---------------------------------------------------------------------------
 template <typename T, int MK, int TW, int NV, int MINB>
 __global__ void __launch_bounds__(TW == 32 ? kWarpTeamBlock : TW, MINB)
 gtms_fwd_vec_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
     constexpr int EPU = 2 * Pairs<T>::kPairs;
-    // Two buffers of (extreme, sum) per warp, alternating per row (a fast warp
-    // could otherwise overwrite a slot a slow warp is still reading).
-    __shared__ float red[2][TW > 32 ? 2 * (TW / 32) : 1];
-    int par = 0;
+    // Per-warp slots of the max and of the sum. A warp writes the max slots of
+    // row k + 1 only after the sum barrier of row k, which every warp reaches
+    // after reading row k's max slots (and likewise for the sum slots).
+    __shared__ float red[TW > 32 ? 2 * (TW / 32) : 1];
+    float* red_max = red;
+    float* red_sum = TW > 32 ? red + TW / 32 : red;
 
     const float c = __fmul_rn(scale, kLog2e);
     const bool use_max = scale >= 0.0f;
@@ -624,22 +624,9 @@ gtms_fwd_vec_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom
 
         float2 v[NV][Pairs<T>::kPairs];
         float ext = fwd_decode_extreme<T, NV>(raw, v, ur, unit_of, use_max);
-        if constexpr (TW >= 1024) {
-            // exps relative to the warp's extreme; one exchange rescales the warps' sums
-            // (saves a CTA-wide round; measured on GB300 it pays only for 1024-thread
-            // teams, +9 % at S = 32768 bf16, and costs 2-5 % for teams of 64-256)
-            ext = use_max ? team_max<32>(ext, nullptr) : -team_max<32>(-ext, nullptr);
-            const float s_w = team_sum<32>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), nullptr);
-            const float f = team_softmax_factor<TW>(ext, s_w, c, use_max, red[par]);
-            par ^= 1;
-            fwd_store<T, NV>(yr, v, ur, unit_of, f);
-        } else {
-            float* red_max = red[0];
-            float* red_sum = TW > 32 ? red[0] + TW / 32 : red[0];
-            ext = use_max ? team_max<TW>(ext, red_max) : -team_max<TW>(-ext, red_max);
-            const float s = team_sum<TW>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), red_sum);
-            fwd_store<T, NV>(yr, v, ur, unit_of, __frcp_rn(s));
-        }
+        ext = use_max ? team_max<TW>(ext, red_max) : -team_max<TW>(-ext, red_max);
+        const float s = team_sum<TW>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), red_sum);
+        fwd_store<T, NV>(yr, v, ur, unit_of, __frcp_rn(s));
     }
 }
 

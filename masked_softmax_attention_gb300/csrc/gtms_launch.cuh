@@ -3,9 +3,9 @@
 
 #include <cuda_runtime.h>
 
-#include "gtms_cluster.cuh"
 #include "gtms_dispatch.h"
 #include "gtms_kernels.cuh"
+#include "gtms_stream.cuh"
 
 namespace gtms {
 
@@ -22,14 +22,6 @@ inline unsigned grid_for(int64_t rows)
 template <int TW>
 constexpr int block_for() { return TW == 32 ? kWarpTeamBlock : TW; }
 
-// Cluster grid: one cluster of C CTAs per row (capped), a multiple of C.
-template <int C>
-inline unsigned cluster_grid_for(int64_t rows)
-{
-    const int64_t cap = int64_t(1) << 26;
-    return static_cast<unsigned>((rows > cap ? cap : rows) * C);
-}
-
 template <typename T, int MK>
 void launch_forward_mk(int id, const void* x, void* y, const int32_t* seq_lens, const Geom& g, float scale,
                        cudaStream_t st)
@@ -40,16 +32,18 @@ void launch_forward_mk(int id, const void* x, void* y, const int32_t* seq_lens, 
     case vid: gtms_fwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
 #define GTMS_FWD_ELEM_CASE(vid, tw, nv) \
     case kElemBase + vid: gtms_fwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
-#define GTMS_FWD_CL_CASE(vid, cl, tw, nv, mb) \
-    case kClusterBase + vid: gtms_fwd_cluster_kernel<T, MK, cl, tw, nv, mb><<<cluster_grid_for<cl>(g.rows), tw, 0, st>>>(xp, yp, seq_lens, g, scale); break;
+#define GTMS_FWD_ST_CASE(vid, tw, nv, mb, mu) \
+    case kStreamBase + vid: gtms_fwd_stream_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), tw, 0, st>>>(xp, yp, seq_lens, g, scale); break;
     if constexpr (sizeof(T) == 4) {
-        switch (id) { GTMS_FWD_VEC4(GTMS_FWD_VEC_CASE) GTMS_ELEM(GTMS_FWD_ELEM_CASE) GTMS_FWD_CL4(GTMS_FWD_CL_CASE) default: break; }
+        switch (id) { GTMS_FWD_VEC4(GTMS_FWD_VEC_CASE) GTMS_ELEM(GTMS_FWD_ELEM_CASE)
+                      GTMS_FWD_ST4(GTMS_FWD_ST_CASE) default: break; }
     } else {
-        switch (id) { GTMS_FWD_VEC2(GTMS_FWD_VEC_CASE) GTMS_ELEM(GTMS_FWD_ELEM_CASE) GTMS_FWD_CL2(GTMS_FWD_CL_CASE) default: break; }
+        switch (id) { GTMS_FWD_VEC2(GTMS_FWD_VEC_CASE) GTMS_ELEM(GTMS_FWD_ELEM_CASE)
+                      GTMS_FWD_ST2(GTMS_FWD_ST_CASE) default: break; }
     }
 #undef GTMS_FWD_VEC_CASE
 #undef GTMS_FWD_ELEM_CASE
-#undef GTMS_FWD_CL_CASE
+#undef GTMS_FWD_ST_CASE
 }
 
 template <typename T, int MK>
@@ -63,16 +57,18 @@ void launch_backward_mk(int id, const void* y, const void* dy, void* dx, const i
     case vid: gtms_bwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
 #define GTMS_BWD_ELEM_CASE(vid, tw, nv) \
     case kElemBase + vid: gtms_bwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
-#define GTMS_BWD_CL_CASE(vid, cl, tw, nv, mb) \
-    case kClusterBase + vid: gtms_bwd_cluster_kernel<T, MK, cl, tw, nv, mb><<<cluster_grid_for<cl>(g.rows), tw, 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
+#define GTMS_BWD_ST_CASE(vid, tw, nv, mb, mu) \
+    case kStreamBase + vid: gtms_bwd_stream_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), tw, 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
     if constexpr (sizeof(T) == 4) {
-        switch (id) { GTMS_BWD_VEC4(GTMS_BWD_VEC_CASE) GTMS_ELEM(GTMS_BWD_ELEM_CASE) GTMS_BWD_CL4(GTMS_BWD_CL_CASE) default: break; }
+        switch (id) { GTMS_BWD_VEC4(GTMS_BWD_VEC_CASE) GTMS_ELEM(GTMS_BWD_ELEM_CASE)
+                      GTMS_BWD_ST4(GTMS_BWD_ST_CASE) default: break; }
     } else {
-        switch (id) { GTMS_BWD_VEC2(GTMS_BWD_VEC_CASE) GTMS_ELEM(GTMS_BWD_ELEM_CASE) GTMS_BWD_CL2(GTMS_BWD_CL_CASE) default: break; }
+        switch (id) { GTMS_BWD_VEC2(GTMS_BWD_VEC_CASE) GTMS_ELEM(GTMS_BWD_ELEM_CASE)
+                      GTMS_BWD_ST2(GTMS_BWD_ST_CASE) default: break; }
     }
 #undef GTMS_BWD_VEC_CASE
 #undef GTMS_BWD_ELEM_CASE
-#undef GTMS_BWD_CL_CASE
+#undef GTMS_BWD_ST_CASE
 }
 
 // One translation unit instantiates one mask kind of one dtype and direction.

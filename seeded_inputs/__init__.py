@@ -26,7 +26,7 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
 * ``s16384_bf16`` -- X[4,8,16384,16384] bf16 ~N(0, variance 4),
   seq_len ~ U{8192..16384}, scale 0.125, and ``s32768_bf16`` --
   X[1,4,32768,32768], seq_len ~ U{16384..32768}: added measurement points for
-  rows split over a cluster of CTAs.
+  rows of 32 KB and more (the two-pass stream kernels).
 * ``attn_s2048_bf16`` -- the attention-backward step at the ``s2048_bf16``
   shape: P the softmax of X[32,16,2048,2048] (bf16, variance 4,
   seq_len ~ U{1024..2048}, scale 0.125), dO and V [32,16,2048,64] ~ N(0,1).
@@ -38,6 +38,8 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
   (P and dS 537 MB each, still larger than L2).
 * ``s1000_b2`` -- X[2,64,1000,1000], otherwise like ``s1000_b12``: a small
   stand-in for profiler captures.
+* ``s32768_m1`` -- X[1,1,32768,32768], otherwise like ``s32768_bf16`` (same
+  seed, same length): one of its four heads, a stand-in for profiler captures.
 
 Every tensor comes from torch's seeded generators (Philox on CUDA, mt19937 on
 the CPU), drawn in float32 and cast to the IO dtype with round-to-nearest-even.
@@ -129,7 +131,7 @@ WORKLOADS = {
                           spike_prob=0.01, spike_value=30.0, seed=20261207),
     "s4096_bf16": Workload("s4096_bf16", 32, 16, 4096, "bf16", 0.125, x_std=2.0,
                            seq_len_range=(2048, 4096), seed=20261208),
-    # rows longer than one CTA holds (a cluster of CTAs per row): added measurement points
+    # rows of 32 KB and more (two-pass stream kernels): added measurement points
     "s16384_bf16": Workload("s16384_bf16", 4, 8, 16384, "bf16", 0.125, x_std=2.0,
                             seq_len_range=(8192, 16384), seed=20261210),
     "s32768_bf16": Workload("s32768_bf16", 1, 4, 32768, "bf16", 0.125, x_std=2.0,
@@ -150,6 +152,10 @@ WORKLOADS = {
     # profiling stand-in for s1000_b12: same distribution, 2 of the 12 batches
     # (2 GB on the device), small enough for a multi-pass ncu capture
     "s1000_b2": Workload("s1000_b2", 2, 64, 1000, "f32", 1.0, seq_len_range=(500, 1000), seed=20261209),
+    # profiling stand-in for s32768_bf16: the same seed, so the same length, one of the 4 heads
+    # (2.1 GB per tensor)
+    "s32768_m1": Workload("s32768_m1", 1, 1, 32768, "bf16", 0.125, x_std=2.0,
+                          seq_len_range=(16384, 32768), seed=20261211),
 }
 
 

@@ -82,19 +82,23 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name(0, 2048, BF16) == "gtms_fwd_vec_kernel<bf16,team64,x4,minb16>"
     assert gtms.kernel_name(1, 2048, BF16) == "gtms_bwd_vec_kernel<bf16,team32,x8,minb5>"
     assert gtms.kernel_name(1, 8192, F16) == "gtms_bwd_vec_kernel<f16,team128,x8,minb0>"
-    assert gtms.kernel_name(0, 8192, F32) == "gtms_fwd_vec_kernel<f32,team512,x4,minb0>"
+    assert gtms.kernel_name(0, 4096, F32) == "gtms_fwd_vec_kernel<f32,team256,x4,minb0>"
     assert gtms.kernel_name(0, 1024, F16) == "gtms_fwd_vec_kernel<f16,team32,x4,minb6>"
+    assert gtms.kernel_name(0, 8200, F16) == "gtms_fwd_vec_kernel<f16,team512,x4,minb2>"
+    assert gtms.kernel_name(0, 16376, BF16) == "gtms_fwd_vec_kernel<bf16,team512,x4,minb2>"   # 32752-byte rows
     # rows whose byte length is not a multiple of 16, or unaligned buffers: element kernels
     assert gtms.kernel_name(0, 5, F32) == "gtms_fwd_elem_kernel<f32,team32,x1>"
     assert gtms.kernel_name(0, 1000, F32, aligned16=False) == "gtms_fwd_elem_kernel<f32,team32,x32>"
     assert gtms.kernel_name(1, 8191, F16) == "gtms_bwd_elem_kernel<f16,team256,x32>"
-    # rows longer than one CTA holds: a cluster of CTAs per row, 16-byte units only
-    assert gtms.kernel_name(0, 16384, F32) == "gtms_fwd_vec_kernel<f32,team1024,x4,minb0>"
-    assert gtms.kernel_name(0, 32768, F32) == "gtms_fwd_cluster_kernel<f32,cluster2,team1024,x4,minb0>"
-    assert gtms.kernel_name(0, 65536, F32) == "gtms_fwd_cluster_kernel<f32,cluster4,team1024,x4,minb0>"
-    assert gtms.kernel_name(1, 65536, BF16) == "gtms_bwd_cluster_kernel<bf16,cluster2,team512,x8,minb0>"
-    assert gtms.kernel_name(1, 32768, BF16) == "gtms_bwd_vec_kernel<bf16,team512,x8,minb0>"
-    assert gtms.kernel_name(0, 8200, F16) == "gtms_fwd_vec_kernel<f16,team512,x4,minb2>"
+    # rows of 32 KB and more: one CTA per row streams the kept units in two passes, 16-byte units only
+    assert gtms.kernel_name(0, 8192, F32) == "gtms_fwd_stream_kernel<f32,team128,x4,minb8>"
+    assert gtms.kernel_name(0, 16384, BF16) == "gtms_fwd_stream_kernel<bf16,team128,x4,minb8>"
+    assert gtms.kernel_name(0, 16384, F32) == "gtms_fwd_stream_kernel<f32,team256,x4,minb4>"
+    assert gtms.kernel_name(0, 32768, BF16) == "gtms_fwd_stream_kernel<bf16,team256,x4,minb4>"
+    assert gtms.kernel_name(0, 65536, F32) == "gtms_fwd_stream_kernel<f32,team256,x4,minb4>"
+    assert gtms.kernel_name(1, 8192, F32) == "gtms_bwd_stream_kernel<f32,team256,x2,minb4>"
+    assert gtms.kernel_name(1, 32768, BF16) == "gtms_bwd_stream_kernel<bf16,team256,x2,minb4>"
+    assert gtms.kernel_name(1, 65536, BF16) == "gtms_bwd_stream_kernel<bf16,team256,x2,minb4>"
     assert gtms.kernel_name(0, 16384, F32, aligned16=False) == "none"
     # out of range
     assert gtms.kernel_name(0, 8193, F32) == "none"

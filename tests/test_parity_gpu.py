@@ -140,7 +140,8 @@ def _kept_mask(lens, M, S, dev):
     return (col[None, None, :] < n[:, :, None])[:, None]                        # [B, 1, S, S]
 
 
-@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5), ("bf16", 33)])
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5), ("bf16", 33),
+                                     ("f32", 8192), ("bf16", 16384)])
 def test_masked_inputs_are_not_read(dev, dtype, S):
     w = si.custom("sentinel", 3, 2, S, dtype, 0.125, seq_lens=(S, S // 2 + 1, 0), seed=21)
     lens = si.seq_lens(w)
@@ -163,7 +164,8 @@ def test_masked_inputs_are_not_read(dev, dtype, S):
                        dx_ref.view(torch.int16 if dtype != "f32" else torch.int32))
 
 
-@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 7)])
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 7), ("f32", 8192),
+                                     ("bf16", 16384)])
 def test_every_output_element_is_written(dev, dtype, S):
     w = si.custom("prefill", 2, 2, S, dtype, 1.0, seq_lens=(S, S // 3), seed=22)
     lens_d = _lens_dev(w, dev)
@@ -180,7 +182,8 @@ def test_every_output_element_is_written(dev, dtype, S):
     assert masked_bits_all_zero(y, lens_d, dtype) and masked_bits_all_zero(dx, lens_d, dtype)
 
 
-@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5)])
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5), ("f32", 8192),
+                                     ("bf16", 16384)])
 def test_exact_aliasing_is_in_place(dev, dtype, S):
     w = si.custom("alias", 2, 3, S, dtype, 0.125, seq_lens=(S, S // 2 + 3), seed=23)
     lens_d = _lens_dev(w, dev)
@@ -201,7 +204,7 @@ def test_exact_aliasing_is_in_place(dev, dtype, S):
 
 
 @pytest.mark.parametrize("offset", [0, 1])
-@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5)])
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5), ("f32", 8192)])
 def test_guard_bands_untouched(dev, dtype, S, offset):
     """Canary bytes around each output stay intact (compute-sanitizer stand-in)."""
     w = si.custom("guard", 2, 2, S, dtype, 1.0, seq_lens=(S, 1), seed=24)
@@ -222,7 +225,7 @@ def test_guard_bands_untouched(dev, dtype, S, offset):
 
 
 def test_row0_is_exactly_one_hot(dev):
-    for dtype, S in (("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5)):
+    for dtype, S in (("f32", 1000), ("bf16", 2048), ("f16", 8192), ("f32", 5), ("f32", 8192), ("bf16", 16384)):
         w = si.custom("row0", 3, 4, S, dtype, 0.37, seq_lens=(S, 1, 2), x_std=3.0, seed=25)
         y = gtms.forward(si.make_x(w, dev), _lens_dev(w, dev), w.scale)
         torch.cuda.synchronize()
@@ -343,7 +346,7 @@ def test_host_pipeline_matches_device_calls(dev, chunk):
 
 
 # ---------------------------------------------------------------------------
-# Rows longer than one CTA holds (8192 < S <= 65536): a cluster of CTAs per row
+# Long rows (up to S = 65536): rows of 32 KB and more stream in two passes, one CTA per row
 # ---------------------------------------------------------------------------
 
 LONG_FULL = [(8200, "f32"), (8200, "bf16"), (12288, "f16"), (16384, "f32"), (16384, "bf16")]
@@ -351,7 +354,7 @@ LONG_FULL = [(8200, "f32"), (8200, "bf16"), (12288, "f16"), (16384, "f32"), (163
 
 @pytest.mark.parametrize("S,dtype", LONG_FULL)
 def test_long_rows_full_comparison(dev, S, dtype):
-    """Every element, lengths S, S//2+1, 1 and 0 (rows spread over 2 or 4 CTAs)."""
+    """Every element, lengths S, S//2+1, 1 and 0 (rows of several stream batches, ragged last batch)."""
     w = si.custom(f"long{S}", 4, 1, S, dtype, 0.125 if dtype != "f32" else 0.7,
                   seq_lens=(S, S // 2 + 1, 1, 0), x_std=2.0, seed=S + 7)
     run_and_check(w, dev)
@@ -360,9 +363,8 @@ def test_long_rows_full_comparison(dev, S, dtype):
 @pytest.mark.parametrize("S,dtype,L", [(32768, "f32", 20001), (32768, "bf16", 32768), (65536, "bf16", 40000),
                                        (65536, "f16", 65536), (65536, "f32", 30001)])
 def test_long_rows_sampled(dev, S, dtype, L):
-    """Largest rows (one 1024-thread CTA up to 64 KB, a cluster of 2 or 4 CTAs
-    beyond): sampled rows element by element, every row's masked bits and live
-    row sums on the device."""
+    """Largest rows (two-pass stream kernels, up to 256 KB rows): sampled rows
+    element by element, every row's masked bits and live row sums on the device."""
     w = si.custom(f"long{S}", 1, 1, S, dtype, 0.125, seq_lens=(L,), seed=S + L)
     lens = si.seq_lens(w)
     lens_d = torch.from_numpy(lens).to(dev)
@@ -393,6 +395,18 @@ def test_long_rows_sampled(dev, S, dtype, L):
     assert sb.ok, f"backward {w.describe()}: {sb}"
     del x, y, dy, dx, y_in
     torch.cuda.empty_cache()
+
+
+SCALE_CASES = [(1000, "f32", -0.7), (2048, "bf16", -0.125), (37, "f16", -2.0), (4096, "f16", -0.25),
+               (8192, "f32", -1.0), (16384, "bf16", -0.125), (1000, "f32", 0.0), (16384, "bf16", 0.0)]
+
+
+@pytest.mark.parametrize("S,dtype,scale", SCALE_CASES)
+def test_negative_and_zero_scale(dev, S, dtype, scale):
+    """scale < 0 makes the row minimum the reference point of the exponentials; scale = 0 gives
+    1/n on every kept element. Warp, CTA, element and stream kernels, forward and backward."""
+    w = si.custom(f"scale{S}", 2, 1, S, dtype, scale, seq_lens=(S, S // 3 + 1), x_std=2.0, seed=S + 31)
+    run_and_check(w, dev)
 
 
 def test_long_rows_that_are_not_16_byte_multiples_are_rejected(dev):
@@ -436,7 +450,7 @@ MASK_CASES = [
 @pytest.mark.parametrize("kind,window,S,dtype", MASK_CASES)
 def test_mask_families(dev, kind, window, S, dtype):
     """Length mask and sliding causal window: every element, head and tail partial units, per-row and
-    cluster kernels, 16-byte and element paths."""
+    stream kernels, 16-byte and element paths."""
     M = 2 if S <= 2048 else 1
     w = si.custom(f"mask{kind}_{S}", 4, M, S, dtype, 0.125 if dtype != "f32" else 1.0,
                   seq_lens=(S, S // 2 + 3, 1, 0), x_std=2.0, seed=S + 31 * kind + window)
