@@ -90,9 +90,9 @@ def entry_points(lib, w):
 
 def kernel_label(gtms, w, direction):
     """Name of the kernel a call of workload w launches (same variant table for every mask)."""
-    name = gtms.kernel_name(direction, w.S, w.dtype_code, True)
     if w.keep_prob > 0:
-        return name.replace("_vec_kernel", "_explicit_kernel")
+        return gtms.kernel_name_explicit(direction, w.S, w.dtype_code)
+    name = gtms.kernel_name(direction, w.S, w.dtype_code, True)
     if w.mask_kind:
         return name.replace(">", f",mask{w.mask_kind}>")
     return name

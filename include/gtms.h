@@ -206,6 +206,14 @@ int gtms_version(void);
  */
 const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16);
 
+/*
+ * Name of the kernel variant that gtms_forward_explicit (direction 0) or
+ * gtms_backward_explicit (direction 1) launches for this row length and dtype
+ * (16-byte-aligned buffers). Static string; "none" for arguments those calls
+ * reject. Host-only, enqueues nothing.
+ */
+const char* gtms_kernel_name_explicit(int direction, int64_t S, int dtype);
+
 #ifdef __cplusplus
 }
 #endif

@@ -469,3 +469,30 @@ GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, in
     return v >= gtms::kElemBase ? names.text[direction][dtype][kMaxRows + v - gtms::kElemBase]
                                 : names.text[direction][dtype][v];
 }
+
+
+GTMS_EXPORT const char* gtms_kernel_name_explicit(int direction, int64_t S, int dtype)
+{
+    static const char* const kDtype[3] = {"f32", "bf16", "f16"};
+    constexpr int kMaxRows = 16;
+    struct Names {
+        char text[2][3][kMaxRows][80];
+        Names()
+        {
+            for (int d = 0; d < 2; ++d)
+                for (int t = 0; t < 3; ++t) {
+                    const gtms::VariantTable vt = gtms::explicit_table(d, t == 0 ? 4 : 2);
+                    for (int i = 0; i < vt.count && i < kMaxRows; ++i)
+                        std::snprintf(text[d][t][i], sizeof text[d][t][i],
+                                      "gtms_%s_explicit_kernel<%s,team%d,x%d,minb%d>", d == 0 ? "fwd" : "bwd",
+                                      kDtype[t], vt.rows[i].team, vt.rows[i].per_thread, vt.rows[i].min_ctas);
+                }
+        }
+    };
+    static const Names names;
+    const int e = elem_bytes(dtype);
+    if ((direction != 0 && direction != 1) || e == 0 || S < 1 || S > 8192 || (S * e) % 16 != 0)
+        return "none";
+    const int v = gtms::pick_variant(direction, S, e, true, false);
+    return v < 0 || v >= kMaxRows ? "none" : names.text[direction][dtype][v];
+}

@@ -37,6 +37,13 @@
                          X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0)
 #define GTMS_BWD_VEC2(X) X(0, 32, 1, 4) X(1, 32, 2, 4) X(2, 32, 4, 4) X(3, 32, 8, 5) \
                          X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0)
+// The explicit-mask forward (gtms_explicit.cuh) takes the same rows with its own
+// register caps: it holds the next head's units besides the current head's
+// exponentials (fp32 warp teams 80 registers, 16-bit teams 78-127).
+#define GTMS_EXF_VEC4(X) X(0, 32, 1, 8) X(1, 32, 2, 8) X(2, 32, 4, 6) X(3, 64, 4, 0) \
+                         X(4, 128, 4, 0) X(5, 256, 4, 0) X(6, 512, 4, 1)
+#define GTMS_EXF_VEC2(X) X(0, 32, 1, 8) X(1, 32, 2, 8) X(2, 32, 4, 5) X(3, 64, 4, 12) \
+                         X(4, 128, 4, 6) X(5, 256, 4, 3) X(6, 512, 4, 1)
 //                       id  team  elements/thread
 #define GTMS_ELEM(X) X(0, 32, 1) X(1, 32, 4) X(2, 32, 16) X(3, 32, 32) X(4, 128, 32) X(5, 256, 32)
 // Stream variants (rows of at least kStreamFromBytes, 16-byte units only):
@@ -64,6 +71,8 @@ constexpr Variant kFwdVec2[] = {GTMS_FWD_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kBwdVec4[] = {GTMS_BWD_VEC4(GTMS_VEC_ROW)};
 constexpr Variant kBwdVec2[] = {GTMS_BWD_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kElem[] = {GTMS_ELEM(GTMS_ELEM_ROW)};
+constexpr Variant kExFwdVec4[] = {GTMS_EXF_VEC4(GTMS_VEC_ROW)};
+constexpr Variant kExFwdVec2[] = {GTMS_EXF_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kFwdSt4[] = {GTMS_FWD_ST4(GTMS_ST_ROW)};
 constexpr Variant kFwdSt2[] = {GTMS_FWD_ST2(GTMS_ST_ROW)};
 constexpr Variant kBwdSt4[] = {GTMS_BWD_ST4(GTMS_ST_ROW)};
@@ -92,6 +101,26 @@ inline VariantTable vec_table(int direction, int elem_bytes)
     if (direction == 0)
         return elem_bytes == 4 ? VariantTable{kFwdVec4, count_of(kFwdVec4)} : VariantTable{kFwdVec2, count_of(kFwdVec2)};
     return elem_bytes == 4 ? VariantTable{kBwdVec4, count_of(kBwdVec4)} : VariantTable{kBwdVec2, count_of(kBwdVec2)};
+}
+
+constexpr bool same_shapes(const Variant* a, const Variant* b, int n)
+{
+    for (int i = 0; i < n; ++i)
+        if (a[i].team != b[i].team || a[i].per_thread != b[i].per_thread)
+            return false;
+    return true;
+}
+static_assert(count_of(kExFwdVec4) == count_of(kFwdVec4) && same_shapes(kExFwdVec4, kFwdVec4, count_of(kFwdVec4)) &&
+                  count_of(kExFwdVec2) == count_of(kFwdVec2) && same_shapes(kExFwdVec2, kFwdVec2, count_of(kFwdVec2)),
+              "explicit-mask forward rows must match the vector rows id for id");
+
+// Variant table of the explicit-mask kernels (same ids as vec_table).
+inline VariantTable explicit_table(int direction, int elem_bytes)
+{
+    if (direction == 0)
+        return elem_bytes == 4 ? VariantTable{kExFwdVec4, count_of(kExFwdVec4)}
+                               : VariantTable{kExFwdVec2, count_of(kExFwdVec2)};
+    return vec_table(direction, elem_bytes);
 }
 
 inline VariantTable stream_table(int direction, int elem_bytes)

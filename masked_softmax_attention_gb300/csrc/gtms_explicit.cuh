@@ -8,8 +8,11 @@
 // row) pair and its M heads: each thread loads the mask bytes of its 16-byte
 // units once (4 bytes per fp32 unit, 8 per 16-bit unit) and keeps the bits
 // for every head; a unit with no kept element loads no x and is stored as
-// +0.0, so masked inputs are still never read. The arithmetic is the vector kernels' (fp32
-// pairs, one ex2.approx.f32 per kept element, float-float backward dot).
+// +0.0, so masked inputs are still never read. The forward loads the next
+// head's kept units as soon as it has decoded the current head's, so those
+// loads are in flight through the current head's two reductions and its
+// stores. The arithmetic is the vector kernels' (fp32 pairs, one
+// ex2.approx.f32 per kept element, float-float backward dot).
 #pragma once
 
 #include "gtms_kernels.cuh"
@@ -73,17 +76,23 @@ gtms_fwd_explicit_kernel(const T* x, T* y, const uint8_t* __restrict__ mask, int
             const int j = tid + k * TW;
             kb[k] = j < g.units ? keep_bits<EPU>(mrow, j) : 0u;
         }
+        // Head 0's kept units; each head then loads the next head's units as
+        // soon as it has decoded its own, so those loads overlap its reductions.
+        Unit16 raw[NV];
+        {
+            const char* x0 = reinterpret_cast<const char*>(x + (static_cast<int64_t>(b) * M * g.S + r) * g.S);
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+                if (kb[k])
+                    raw[k] = load16(x0 + 16 * (tid + k * TW));
+        }
       for (int32_t m = 0; m < M; ++m) {
         const int64_t q = (static_cast<int64_t>(b) * M + m) * g.S + r;
-        const char* xr = reinterpret_cast<const char*>(x + q * g.S);
         char* yr = reinterpret_cast<char*>(y + q * g.S);
-        Unit16 raw[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             const int j = tid + k * TW;
-            if (kb[k])
-                raw[k] = load16(xr + 16 * j);
-            else if (j < g.units)
+            if (!kb[k] && j < g.units)
                 store16(yr + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
         }
 
@@ -102,6 +111,13 @@ gtms_fwd_explicit_kernel(const T* x, T* y, const uint8_t* __restrict__ mask, int
                     ext = use_max ? max3(ext, v[k][p].x, v[k][p].y) : min3(ext, v[k][p].x, v[k][p].y);
                 }
             }
+        }
+        if (m + 1 < M) {   // the next head's row is S rows further on
+            const char* xn = reinterpret_cast<const char*>(x + (q + g.S) * g.S);
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+                if (kb[k])
+                    raw[k] = load16(xn + 16 * (tid + k * TW));
         }
         ext = use_max ? team_max<TW>(ext, red) : -team_max<TW>(-ext, red);
 
@@ -236,7 +252,8 @@ gtms_bwd_explicit_kernel(const T* y, const T* dy, T* dx, const uint8_t* __restri
 
 namespace gtms {
 
-// Explicit-mask launchers: the per-row vector variants of gtms_dispatch.h.
+// Explicit-mask launchers: the per-row vector variants of gtms_dispatch.h (the
+// forward with its own register caps, GTMS_EXF_VEC*).
 template <typename T>
 void launch_forward_explicit(int id, const void* x, void* y, const uint8_t* mask, int32_t mask_batches, const Geom& g,
                              float scale, cudaStream_t st)
@@ -246,9 +263,9 @@ void launch_forward_explicit(int id, const void* x, void* y, const uint8_t* mask
 #define GTMS_EX_FWD_CASE(vid, tw, nv, mb) \
     case vid: gtms_fwd_explicit_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows / (g.rows_per_b / g.S)), block_for<tw>(), 0, st>>>(xp, yp, mask, mask_batches, g, scale); break;
     if constexpr (sizeof(T) == 4) {
-        switch (id) { GTMS_FWD_VEC4(GTMS_EX_FWD_CASE) default: break; }
+        switch (id) { GTMS_EXF_VEC4(GTMS_EX_FWD_CASE) default: break; }
     } else {
-        switch (id) { GTMS_FWD_VEC2(GTMS_EX_FWD_CASE) default: break; }
+        switch (id) { GTMS_EXF_VEC2(GTMS_EX_FWD_CASE) default: break; }
     }
 #undef GTMS_EX_FWD_CASE
 }

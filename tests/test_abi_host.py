@@ -100,6 +100,13 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name(1, 32768, BF16) == "gtms_bwd_stream_kernel<bf16,team256,x2,minb4>"
     assert gtms.kernel_name(1, 65536, BF16) == "gtms_bwd_stream_kernel<bf16,team256,x2,minb4>"
     assert gtms.kernel_name(0, 16384, F32, aligned16=False) == "none"
+    # explicit-mask kernels: the vector rows, the forward with its own register caps, up to S = 8192
+    assert gtms.kernel_name_explicit(0, 2048, BF16) == "gtms_fwd_explicit_kernel<bf16,team64,x4,minb12>"
+    assert gtms.kernel_name_explicit(1, 2048, BF16) == "gtms_bwd_explicit_kernel<bf16,team32,x8,minb5>"
+    assert gtms.kernel_name_explicit(0, 1000, F32) == "gtms_fwd_explicit_kernel<f32,team64,x4,minb0>"
+    assert gtms.kernel_name_explicit(0, 8192, F32) == "gtms_fwd_explicit_kernel<f32,team512,x4,minb1>"
+    assert gtms.kernel_name_explicit(0, 16384, BF16) == "none"
+    assert gtms.kernel_name_explicit(0, 1001, F32) == "none"
     # out of range
     assert gtms.kernel_name(0, 8193, F32) == "none"
     assert gtms.kernel_name(0, 65537, BF16) == "none"
