@@ -92,10 +92,7 @@ def kernel_label(gtms, w, direction):
     """Name of the kernel a call of workload w launches (same variant table for every mask)."""
     if w.keep_prob > 0:
         return gtms.kernel_name_explicit(direction, w.S, w.dtype_code)
-    name = gtms.kernel_name(direction, w.S, w.dtype_code, True)
-    if w.mask_kind:
-        return name.replace(">", f",mask{w.mask_kind}>")
-    return name
+    return gtms.kernel_name_masked(direction, w.S, w.dtype_code, w.mask_kind, w.window)
 
 
 # ---------------------------------------------------------------------------

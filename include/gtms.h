@@ -207,6 +207,17 @@ int gtms_version(void);
 const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16);
 
 /*
+ * Name of the kernel variant that gtms_forward_masked (direction 0) or
+ * gtms_backward_masked (direction 1) launches for this row length, dtype,
+ * alignment, mask kind and window. Mask kinds 1 and 2 append ",maskK" to the
+ * per-row kernel's name; a narrow sliding window may take a band kernel
+ * instead. Static string; "none" for unsupported arguments. Host-only,
+ * enqueues nothing.
+ */
+const char* gtms_kernel_name_masked(int direction, int64_t S, int dtype, int aligned16, int mask_kind,
+                                    int64_t window);
+
+/*
  * Name of the kernel variant that gtms_forward_explicit (direction 0) or
  * gtms_backward_explicit (direction 1) launches for this row length and dtype
  * (16-byte-aligned buffers). Static string; "none" for arguments those calls

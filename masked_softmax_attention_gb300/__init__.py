@@ -27,7 +27,8 @@ GTMS_MAX_S = 65536
 GTMS_MASK_GROUPED_TRIL, GTMS_MASK_LENGTH, GTMS_MASK_SLIDING_WINDOW = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("gtms_forward", "gtms_backward", "gtms_status_string", "gtms_version",
-                    "gtms_kernel_name", "gtms_kernel_name_explicit", "gtms_device_pointer_of_host",
+                    "gtms_kernel_name", "gtms_kernel_name_masked", "gtms_kernel_name_explicit",
+                    "gtms_device_pointer_of_host",
                     "gtms_forward_masked",
                     "gtms_backward_masked", "gtms_forward_explicit", "gtms_backward_explicit",
                     "gtms_attention_softmax_backward")
@@ -80,6 +81,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.gtms_version.restype = ctypes.c_int
         lib.gtms_kernel_name.argtypes = [ctypes.c_int, i64, ctypes.c_int, ctypes.c_int]
         lib.gtms_kernel_name.restype = ctypes.c_char_p
+        lib.gtms_kernel_name_masked.argtypes = [ctypes.c_int, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, i64]
+        lib.gtms_kernel_name_masked.restype = ctypes.c_char_p
         lib.gtms_kernel_name_explicit.argtypes = [ctypes.c_int, i64, ctypes.c_int]
         lib.gtms_kernel_name_explicit.restype = ctypes.c_char_p
         lib.gtms_device_pointer_of_host.argtypes = [vp, ctypes.POINTER(ctypes.c_void_p)]
@@ -133,6 +136,12 @@ def gtms_version() -> int:
 
 def kernel_name(direction: int, S: int, dtype: int, aligned16: bool = True) -> str:
     return load_library().gtms_kernel_name(direction, S, dtype, 1 if aligned16 else 0).decode()
+
+
+def kernel_name_masked(direction: int, S: int, dtype: int, mask_kind: int, window: int = 0,
+                       aligned16: bool = True) -> str:
+    return load_library().gtms_kernel_name_masked(direction, S, dtype, 1 if aligned16 else 0, mask_kind,
+                                                  window).decode()
 
 
 def kernel_name_explicit(direction: int, S: int, dtype: int) -> str:

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -217,7 +218,8 @@ GTMS_EXPORT int gtms_forward_masked(const void* x, void* y, const int32_t* seq_l
         return GTMS_ERR_INVALID_ARG;
 
     const bool a16 = aligned_to(x, 16) && aligned_to(y, 16);
-    const int variant = gtms::pick_variant(0, S, e, a16);
+    const int band = mask_kind == GTMS_MASK_SLIDING_WINDOW ? gtms::pick_band_variant(0, S, e, a16, window) : -1;
+    const int variant = band >= 0 ? band : gtms::pick_variant(0, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
     const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e, window);
@@ -256,7 +258,8 @@ GTMS_EXPORT int gtms_backward_masked(const void* y, const void* dy, void* dx, co
         return GTMS_ERR_INVALID_ARG;
 
     const bool a16 = aligned_to(y, 16) && aligned_to(dy, 16) && aligned_to(dx, 16);
-    const int variant = gtms::pick_variant(1, S, e, a16);
+    const int band = mask_kind == GTMS_MASK_SLIDING_WINDOW ? gtms::pick_band_variant(1, S, e, a16, window) : -1;
+    const int variant = band >= 0 ? band : gtms::pick_variant(1, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
     const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e, window);
@@ -428,48 +431,85 @@ GTMS_EXPORT const char* gtms_status_string(int status)
 
 GTMS_EXPORT int gtms_version(void) { return GTMS_VERSION; }
 
-GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16)
-{
-    static const char* const kDtype[3] = {"f32", "bf16", "f16"};
-    constexpr int kMaxRows = 16;
-    // [direction][dtype][vector, element, stream rows], filled once (thread-safe static init).
-    struct Names {
-        char text[2][3][3 * kMaxRows][80];
-        Names()
-        {
-            for (int d = 0; d < 2; ++d)
-                for (int t = 0; t < 3; ++t) {
+namespace {
+
+// Names of every kernel variant, filled once (thread-safe static init):
+// [direction][dtype][mask kind][slot], slot = table row + kSlots * family
+// (per-row vector, element, stream, band). Mask kinds 1 and 2 append ",maskK".
+struct KernelNames {
+    static constexpr int kSlots = 16;
+    char text[2][3][3][4 * kSlots][96];
+
+    KernelNames()
+    {
+        static const char* const kDtype[3] = {"f32", "bf16", "f16"};
+        for (int d = 0; d < 2; ++d)
+            for (int t = 0; t < 3; ++t)
+                for (int mk = 0; mk < 3; ++mk) {
+                    char suffix[16] = "";
+                    if (mk != 0)
+                        std::snprintf(suffix, sizeof suffix, ",mask%d", mk);
+                    const char* dir = d == 0 ? "fwd" : "bwd";
                     const int e = t == 0 ? 4 : 2;
                     const gtms::VariantTable vt = gtms::vec_table(d, e);
-                    for (int i = 0; i < vt.count && i < kMaxRows; ++i)
-                        std::snprintf(text[d][t][i], sizeof text[d][t][i], "gtms_%s_vec_kernel<%s,team%d,x%d,minb%d>",
-                                      d == 0 ? "fwd" : "bwd", kDtype[t], vt.rows[i].team, vt.rows[i].per_thread,
-                                      vt.rows[i].min_ctas);
-                    for (int i = 0; i < gtms::count_of(gtms::kElem) && i < kMaxRows; ++i)
-                        std::snprintf(text[d][t][kMaxRows + i], sizeof text[d][t][kMaxRows + i],
-                                      "gtms_%s_elem_kernel<%s,team%d,x%d>", d == 0 ? "fwd" : "bwd", kDtype[t],
-                                      gtms::kElem[i].team, gtms::kElem[i].per_thread);
+                    for (int i = 0; i < vt.count && i < kSlots; ++i)
+                        std::snprintf(text[d][t][mk][i], 96, "gtms_%s_vec_kernel<%s,team%d,x%d,minb%d%s>", dir,
+                                      kDtype[t], vt.rows[i].team, vt.rows[i].per_thread, vt.rows[i].min_ctas, suffix);
+                    for (int i = 0; i < gtms::count_of(gtms::kElem) && i < kSlots; ++i)
+                        std::snprintf(text[d][t][mk][kSlots + i], 96, "gtms_%s_elem_kernel<%s,team%d,x%d%s>", dir,
+                                      kDtype[t], gtms::kElem[i].team, gtms::kElem[i].per_thread, suffix);
                     const gtms::VariantTable st = gtms::stream_table(d, e);
-                    for (int i = 0; i < st.count && i < kMaxRows; ++i)
-                        std::snprintf(text[d][t][2 * kMaxRows + i], sizeof text[d][t][2 * kMaxRows + i],
-                                      "gtms_%s_stream_kernel<%s,team%d,x%d,minb%d>", d == 0 ? "fwd" : "bwd", kDtype[t],
-                                      st.rows[i].team, st.rows[i].per_thread, st.rows[i].min_ctas);
+                    for (int i = 0; i < st.count && i < kSlots; ++i)
+                        std::snprintf(text[d][t][mk][2 * kSlots + i], 96, "gtms_%s_stream_kernel<%s,team%d,x%d,minb%d%s>",
+                                      dir, kDtype[t], st.rows[i].team, st.rows[i].per_thread, st.rows[i].min_ctas,
+                                      suffix);
+                    const gtms::VariantTable bt = gtms::band_table(d);
+                    for (int i = 0; i < bt.count && i < kSlots; ++i)
+                        std::snprintf(text[d][t][mk][3 * kSlots + i], 96, "gtms_%s_band_kernel<%s,x%d,minb%d>", dir,
+                                      kDtype[t], bt.rows[i].per_thread, bt.rows[i].min_ctas);
                 }
-        }
-    };
-    static const Names names;
-    const int e = elem_bytes(dtype);
-    if ((direction != 0 && direction != 1) || e == 0 || S < 1 || S > GTMS_MAX_S)
-        return "none";
-    const int v = gtms::pick_variant(direction, S, e, aligned16 != 0);
-    if (v < 0)
-        return "none";
-    if (v >= gtms::kStreamBase)
-        return names.text[direction][dtype][2 * kMaxRows + v - gtms::kStreamBase];
-    return v >= gtms::kElemBase ? names.text[direction][dtype][kMaxRows + v - gtms::kElemBase]
-                                : names.text[direction][dtype][v];
+    }
+
+    const char* of(int direction, int dtype, int mask_kind, int variant) const
+    {
+        int slot;
+        if (variant >= gtms::kBandBase)
+            slot = 3 * kSlots + variant - gtms::kBandBase;
+        else if (variant >= gtms::kStreamBase)
+            slot = 2 * kSlots + variant - gtms::kStreamBase;
+        else if (variant >= gtms::kElemBase)
+            slot = kSlots + variant - gtms::kElemBase;
+        else
+            slot = variant;
+        return text[direction][dtype][mask_kind][slot];
+    }
+};
+
+const KernelNames& kernel_names()
+{
+    static const KernelNames names;
+    return names;
 }
 
+}  // namespace
+
+GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16)
+{
+    return gtms_kernel_name_masked(direction, S, dtype, aligned16, GTMS_MASK_GROUPED_TRIL, 0);
+}
+
+GTMS_EXPORT const char* gtms_kernel_name_masked(int direction, int64_t S, int dtype, int aligned16, int mask_kind,
+                                                int64_t window)
+{
+    const int e = elem_bytes(dtype);
+    if ((direction != 0 && direction != 1) || e == 0 || S < 1 || S > GTMS_MAX_S || check_mask(mask_kind, window))
+        return "none";
+    int v = mask_kind == GTMS_MASK_SLIDING_WINDOW ? gtms::pick_band_variant(direction, S, e, aligned16 != 0, window)
+                                                  : -1;
+    if (v < 0)
+        v = gtms::pick_variant(direction, S, e, aligned16 != 0);
+    return v < 0 ? "none" : kernel_names().of(direction, dtype, mask_kind, v);
+}
 
 GTMS_EXPORT const char* gtms_kernel_name_explicit(int direction, int64_t S, int dtype)
 {

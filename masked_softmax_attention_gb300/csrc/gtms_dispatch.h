@@ -46,6 +46,12 @@
                          X(4, 128, 4, 6) X(5, 256, 4, 3) X(6, 512, 4, 1)
 //                       id  team  elements/thread
 #define GTMS_ELEM(X) X(0, 32, 1) X(1, 32, 4) X(2, 32, 16) X(3, 32, 32) X(4, 128, 32) X(5, 256, 32)
+// Band variants (sliding-window rows whose window spans at most 32 * KV units,
+// in rows longer than one warp's 128 units; 16-byte units only, below the
+// stream rows): a warp owns a row and holds only the window (gtms_band.cuh).
+//                        id  units/lane  min CTAs/SM
+#define GTMS_FWD_BAND(X) X(0, 1, 8) X(1, 2, 8) X(2, 4, 6)
+#define GTMS_BWD_BAND(X) X(0, 1, 4) X(1, 2, 4) X(2, 4, 4) X(3, 8, 5)
 // Stream variants (rows of at least kStreamFromBytes, 16-byte units only):
 //                      id  team  units/thread per batch  min CTAs/SM  max row units
 #define GTMS_FWD_ST4(X) X(0, 128, 4, 8, 4095) X(1, 256, 4, 4, INT32_MAX)
@@ -66,11 +72,14 @@ struct Variant {
 #define GTMS_VEC_ROW(id, tw, nv, mb) {tw, nv, mb, true, (tw) * (nv)},
 #define GTMS_ELEM_ROW(id, tw, nv) {tw, nv, 0, false, (tw) * (nv)},
 #define GTMS_ST_ROW(id, tw, nv, mb, mu) {tw, nv, mb, true, mu},
+#define GTMS_BAND_ROW(id, nv, mb) {32, nv, mb, true, 32 * (nv)},
 constexpr Variant kFwdVec4[] = {GTMS_FWD_VEC4(GTMS_VEC_ROW)};
 constexpr Variant kFwdVec2[] = {GTMS_FWD_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kBwdVec4[] = {GTMS_BWD_VEC4(GTMS_VEC_ROW)};
 constexpr Variant kBwdVec2[] = {GTMS_BWD_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kElem[] = {GTMS_ELEM(GTMS_ELEM_ROW)};
+constexpr Variant kFwdBand[] = {GTMS_FWD_BAND(GTMS_BAND_ROW)};
+constexpr Variant kBwdBand[] = {GTMS_BWD_BAND(GTMS_BAND_ROW)};
 constexpr Variant kExFwdVec4[] = {GTMS_EXF_VEC4(GTMS_VEC_ROW)};
 constexpr Variant kExFwdVec2[] = {GTMS_EXF_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kFwdSt4[] = {GTMS_FWD_ST4(GTMS_ST_ROW)};
@@ -80,12 +89,14 @@ constexpr Variant kBwdSt2[] = {GTMS_BWD_ST2(GTMS_ST_ROW)};
 #undef GTMS_VEC_ROW
 #undef GTMS_ELEM_ROW
 #undef GTMS_ST_ROW
+#undef GTMS_BAND_ROW
 
 template <typename V, int N>
 constexpr int count_of(const V (&)[N]) { return N; }
 
 constexpr int kElemBase = 100;     // variant ids in [kElemBase, kStreamBase) are element variants
-constexpr int kStreamBase = 300;   // variant ids >= kStreamBase are stream variants
+constexpr int kStreamBase = 300;   // variant ids in [kStreamBase, kBandBase) are stream variants
+constexpr int kBandBase = 400;     // variant ids >= kBandBase are band variants
 
 // Row byte length from which the stream variants serve a row, per direction
 // (forward, backward).
@@ -158,8 +169,38 @@ inline int pick_variant(int direction, int64_t S, int elem_bytes, bool aligned16
     return -1;
 }
 
+inline VariantTable band_table(int direction)
+{
+    return direction == 0 ? VariantTable{kFwdBand, count_of(kFwdBand)} : VariantTable{kBwdBand, count_of(kBwdBand)};
+}
+
+// Band variant id for a sliding window of `window` columns, or -1 when the
+// row-length variant (pick_variant) serves the row better: the window must fit
+// a warp's slots, and the row must be a 16-byte-unit row longer than 128 units
+// that is not a stream row.
+inline int pick_band_variant(int direction, int64_t S, int elem_bytes, bool aligned16, int64_t window)
+{
+    if (S <= 0 || window < 1 || !aligned16 || (S * elem_bytes) % 16 != 0)
+        return -1;
+    const int64_t units = S * elem_bytes / 16;
+    if (units <= 128 || S * elem_bytes >= kStreamFromBytes[direction])
+        return -1;
+    const int64_t epu = 16 / elem_bytes;
+    const int64_t w = window < S ? window : S;
+    const int64_t spanned = (w + 2 * epu - 2) / epu;   // units a run of w columns can touch
+    if (2 * spanned > units)
+        return -1;
+    const VariantTable t = band_table(direction);
+    for (int i = 0; i < t.count; ++i)
+        if (spanned <= t.rows[i].max_units)
+            return kBandBase + i;
+    return -1;
+}
+
 inline Variant variant_at(int direction, int elem_bytes, int id)
 {
+    if (id >= kBandBase)
+        return band_table(direction).rows[id - kBandBase];
     if (id >= kStreamBase)
         return stream_table(direction, elem_bytes).rows[id - kStreamBase];
     if (id >= kElemBase)

@@ -5,6 +5,7 @@
 
 #include "gtms_dispatch.h"
 #include "gtms_kernels.cuh"
+#include "gtms_band.cuh"
 #include "gtms_stream.cuh"
 
 namespace gtms {
@@ -32,6 +33,14 @@ void launch_forward_mk(int id, const void* x, void* y, const int32_t* seq_lens, 
     case vid: gtms_fwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
 #define GTMS_FWD_ELEM_CASE(vid, tw, nv) \
     case kElemBase + vid: gtms_fwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
+#define GTMS_FWD_BAND_CASE(vid, nv, mb) \
+    case kBandBase + vid: gtms_fwd_band_kernel<T, nv, mb><<<grid_for<32>(g.rows), block_for<32>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
+    if constexpr (MK == kMaskWindow) {
+        switch (id) { GTMS_FWD_BAND(GTMS_FWD_BAND_CASE) default: break; }
+        if (id >= kBandBase)
+            return;
+    }
+#undef GTMS_FWD_BAND_CASE
 #define GTMS_FWD_ST_CASE(vid, tw, nv, mb, mu) \
     case kStreamBase + vid: gtms_fwd_stream_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), tw, 0, st>>>(xp, yp, seq_lens, g, scale); break;
     if constexpr (sizeof(T) == 4) {
@@ -57,6 +66,14 @@ void launch_backward_mk(int id, const void* y, const void* dy, void* dx, const i
     case vid: gtms_bwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
 #define GTMS_BWD_ELEM_CASE(vid, tw, nv) \
     case kElemBase + vid: gtms_bwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
+#define GTMS_BWD_BAND_CASE(vid, nv, mb) \
+    case kBandBase + vid: gtms_bwd_band_kernel<T, nv, mb><<<grid_for<32>(g.rows), block_for<32>(), 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
+    if constexpr (MK == kMaskWindow) {
+        switch (id) { GTMS_BWD_BAND(GTMS_BWD_BAND_CASE) default: break; }
+        if (id >= kBandBase)
+            return;
+    }
+#undef GTMS_BWD_BAND_CASE
 #define GTMS_BWD_ST_CASE(vid, tw, nv, mb, mu) \
     case kStreamBase + vid: gtms_bwd_stream_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), tw, 0, st>>>(yp, gp, dp, seq_lens, g, scale); break;
     if constexpr (sizeof(T) == 4) {

@@ -100,6 +100,21 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name(1, 32768, BF16) == "gtms_bwd_stream_kernel<bf16,team256,x2,minb4>"
     assert gtms.kernel_name(1, 65536, BF16) == "gtms_bwd_stream_kernel<bf16,team256,x2,minb4>"
     assert gtms.kernel_name(0, 16384, F32, aligned16=False) == "none"
+    # mask families: the row-length variant with the mask kind, or a warp-per-row band kernel for a
+    # narrow sliding window in a row longer than one warp's 128 units
+    assert gtms.kernel_name_masked(0, 2048, BF16, 1) == "gtms_fwd_vec_kernel<bf16,team64,x4,minb16,mask1>"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 0) == gtms.kernel_name(0, 2048, BF16)
+    assert gtms.kernel_name_masked(0, 2048, BF16, 2, 256) == "gtms_fwd_band_kernel<bf16,x2,minb8>"
+    assert gtms.kernel_name_masked(1, 2048, BF16, 2, 256) == "gtms_bwd_band_kernel<bf16,x2,minb4>"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 2, 100) == "gtms_fwd_band_kernel<bf16,x1,minb8>"
+    assert gtms.kernel_name_masked(0, 8192, F16, 2, 300) == "gtms_fwd_band_kernel<f16,x2,minb8>"
+    assert gtms.kernel_name_masked(1, 1000, F32, 2, 1000) == "gtms_bwd_vec_kernel<f32,team32,x8,minb5,mask2>"
+    assert gtms.kernel_name_masked(0, 1000, F32, 2, 7) == "gtms_fwd_band_kernel<f32,x1,minb8>"
+    assert gtms.kernel_name_masked(0, 512, F32, 2, 7) == "gtms_fwd_vec_kernel<f32,team32,x4,minb8,mask2>"
+    assert gtms.kernel_name_masked(0, 1000, F32, 2, 7, aligned16=False) == "gtms_fwd_elem_kernel<f32,team32,x32,mask2>"
+    assert gtms.kernel_name_masked(0, 16384, F32, 2, 5000) == "gtms_fwd_stream_kernel<f32,team256,x4,minb4,mask2>"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 2, 0) == "none"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 3, 1) == "none"
     # explicit-mask kernels: the vector rows, the forward with its own register caps, up to S = 8192
     assert gtms.kernel_name_explicit(0, 2048, BF16) == "gtms_fwd_explicit_kernel<bf16,team64,x4,minb12>"
     assert gtms.kernel_name_explicit(1, 2048, BF16) == "gtms_bwd_explicit_kernel<bf16,team32,x8,minb5>"

@@ -444,6 +444,7 @@ MASK_CASES = [
     (1, 0, 1000, "f32"), (1, 0, 2048, "bf16"), (1, 0, 37, "f16"), (1, 0, 8192, "f16"), (1, 0, 16384, "bf16"),
     (2, 1, 1000, "f32"), (2, 7, 1000, "f32"), (2, 100, 2048, "bf16"), (2, 257, 33, "f16"), (2, 300, 8192, "f16"),
     (2, 5000, 16384, "f32"), (2, 8, 64, "bf16"), (2, 9, 5, "f32"),
+    (2, 900, 4096, "bf16"), (2, 1500, 8192, "f16"), (2, 256, 2048, "bf16"),
 ]
 
 
@@ -455,6 +456,15 @@ def test_mask_families(dev, kind, window, S, dtype):
     w = si.custom(f"mask{kind}_{S}", 4, M, S, dtype, 0.125 if dtype != "f32" else 1.0,
                   seq_lens=(S, S // 2 + 3, 1, 0), x_std=2.0, seed=S + 31 * kind + window)
     run_and_check(w, dev, mask_kind=kind, window=window)
+
+
+@pytest.mark.parametrize("S,dtype,window,scale", [(2048, "bf16", 256, -0.125), (1000, "f32", 7, 0.0),
+                                                  (4096, "f16", 129, -0.5)])
+def test_band_kernels_negative_and_zero_scale(dev, S, dtype, window, scale):
+    """Narrow sliding windows (warp-per-row band kernels) with the row minimum as the reference point
+    (scale < 0) and with scale = 0 (1/n on every kept element)."""
+    w = si.custom(f"band{S}", 3, 2, S, dtype, scale, seq_lens=(S, S // 2 + 5, 1), x_std=2.0, seed=S + window)
+    run_and_check(w, dev, mask_kind=2, window=window)
 
 
 def test_mask_family_sentinels_and_aliasing(dev):
