@@ -219,7 +219,7 @@ GTMS_EXPORT int gtms_forward_masked(const void* x, void* y, const int32_t* seq_l
 
     const bool a16 = aligned_to(x, 16) && aligned_to(y, 16);
     const int band = mask_kind == GTMS_MASK_SLIDING_WINDOW ? gtms::pick_band_variant(0, S, e, a16, window) : -1;
-    const int variant = band >= 0 ? band : gtms::pick_variant(0, S, e, a16);
+    const int variant = band >= 0 ? band : gtms::pick_launch_variant(0, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
     const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e, window);
@@ -259,7 +259,7 @@ GTMS_EXPORT int gtms_backward_masked(const void* y, const void* dy, void* dx, co
 
     const bool a16 = aligned_to(y, 16) && aligned_to(dy, 16) && aligned_to(dx, 16);
     const int band = mask_kind == GTMS_MASK_SLIDING_WINDOW ? gtms::pick_band_variant(1, S, e, a16, window) : -1;
-    const int variant = band >= 0 ? band : gtms::pick_variant(1, S, e, a16);
+    const int variant = band >= 0 ? band : gtms::pick_launch_variant(1, S, e, a16);
     if (variant < 0)
         return GTMS_ERR_UNSUPPORTED;
     const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e, window);
@@ -435,10 +435,11 @@ namespace {
 
 // Names of every kernel variant, filled once (thread-safe static init):
 // [direction][dtype][mask kind][slot], slot = table row + kSlots * family
-// (per-row vector, element, stream, band). Mask kinds 1 and 2 append ",maskK".
+// (per-row vector, element, stream, band, heads). Mask kinds 1 and 2 append
+// ",maskK".
 struct KernelNames {
     static constexpr int kSlots = 16;
-    char text[2][3][3][4 * kSlots][96];
+    char text[2][3][3][5 * kSlots][96];
 
     KernelNames()
     {
@@ -463,6 +464,11 @@ struct KernelNames {
                         std::snprintf(text[d][t][mk][2 * kSlots + i], 96, "gtms_%s_stream_kernel<%s,team%d,x%d,minb%d%s>",
                                       dir, kDtype[t], st.rows[i].team, st.rows[i].per_thread, st.rows[i].min_ctas,
                                       suffix);
+                    const gtms::VariantTable ht = gtms::heads_table();
+                    for (int i = 0; i < ht.count && gtms::kFwdHeads2Ids[i] < kSlots; ++i)
+                        std::snprintf(text[d][t][mk][4 * kSlots + gtms::kFwdHeads2Ids[i]], 96,
+                                      "gtms_%s_heads_kernel<%s,team%d,x%d,minb%d%s>", dir, kDtype[t], ht.rows[i].team,
+                                      ht.rows[i].per_thread, ht.rows[i].min_ctas, suffix);
                     const gtms::VariantTable bt = gtms::band_table(d);
                     for (int i = 0; i < bt.count && i < kSlots; ++i)
                         std::snprintf(text[d][t][mk][3 * kSlots + i], 96, "gtms_%s_band_kernel<%s,x%d,minb%d>", dir,
@@ -473,7 +479,9 @@ struct KernelNames {
     const char* of(int direction, int dtype, int mask_kind, int variant) const
     {
         int slot;
-        if (variant >= gtms::kBandBase)
+        if (variant >= gtms::kHeadsBase)
+            slot = 4 * kSlots + variant - gtms::kHeadsBase;
+        else if (variant >= gtms::kBandBase)
             slot = 3 * kSlots + variant - gtms::kBandBase;
         else if (variant >= gtms::kStreamBase)
             slot = 2 * kSlots + variant - gtms::kStreamBase;
@@ -507,7 +515,7 @@ GTMS_EXPORT const char* gtms_kernel_name_masked(int direction, int64_t S, int dt
     int v = mask_kind == GTMS_MASK_SLIDING_WINDOW ? gtms::pick_band_variant(direction, S, e, aligned16 != 0, window)
                                                   : -1;
     if (v < 0)
-        v = gtms::pick_variant(direction, S, e, aligned16 != 0);
+        v = gtms::pick_launch_variant(direction, S, e, aligned16 != 0);
     return v < 0 ? "none" : kernel_names().of(direction, dtype, mask_kind, v);
 }
 

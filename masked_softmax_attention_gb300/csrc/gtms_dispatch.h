@@ -37,6 +37,13 @@
                          X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0)
 #define GTMS_BWD_VEC2(X) X(0, 32, 1, 4) X(1, 32, 2, 4) X(2, 32, 4, 4) X(3, 32, 8, 5) \
                          X(4, 64, 8, 0) X(5, 128, 8, 0) X(6, 256, 8, 0)
+// 16-bit forward rows served by a CTA team run as heads kernels (a team per
+// (batch, row) pair, next head's loads issued early; gtms_kernels.cuh), with
+// their own register caps. Measured on GB300 against one row per team: S = 2048
+// bf16 5.86 -> 6.40 TB/s, S = 4096 bf16 5.82 -> 6.49, S = 8192 fp16 5.66 ->
+// 6.41; for fp32 rows (S = 1000: 6.53 -> 6.21) one row per team stays ahead.
+//                         id  team  units/thread  min CTAs/SM  (ids of GTMS_FWD_VEC2)
+#define GTMS_FWD_HEADS2(X) X(3, 64, 4, 12) X(4, 128, 4, 6) X(5, 256, 4, 3) X(6, 512, 4, 1)
 // The explicit-mask forward (gtms_explicit.cuh) takes the same rows with its own
 // register caps: it holds the next head's units besides the current head's
 // exponentials (fp32 warp teams 80 registers, 16-bit teams 78-127).
@@ -78,6 +85,12 @@ constexpr Variant kFwdVec2[] = {GTMS_FWD_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kBwdVec4[] = {GTMS_BWD_VEC4(GTMS_VEC_ROW)};
 constexpr Variant kBwdVec2[] = {GTMS_BWD_VEC2(GTMS_VEC_ROW)};
 constexpr Variant kElem[] = {GTMS_ELEM(GTMS_ELEM_ROW)};
+#define GTMS_HEADS_ROW(id, tw, nv, mb) {tw, nv, mb, true, (tw) * (nv)},
+constexpr Variant kFwdHeads2[] = {GTMS_FWD_HEADS2(GTMS_HEADS_ROW)};
+#undef GTMS_HEADS_ROW
+#define GTMS_HEADS_ID(id, tw, nv, mb) id,
+constexpr int kFwdHeads2Ids[] = {GTMS_FWD_HEADS2(GTMS_HEADS_ID)};
+#undef GTMS_HEADS_ID
 constexpr Variant kFwdBand[] = {GTMS_FWD_BAND(GTMS_BAND_ROW)};
 constexpr Variant kBwdBand[] = {GTMS_BWD_BAND(GTMS_BAND_ROW)};
 constexpr Variant kExFwdVec4[] = {GTMS_EXF_VEC4(GTMS_VEC_ROW)};
@@ -96,7 +109,8 @@ constexpr int count_of(const V (&)[N]) { return N; }
 
 constexpr int kElemBase = 100;     // variant ids in [kElemBase, kStreamBase) are element variants
 constexpr int kStreamBase = 300;   // variant ids in [kStreamBase, kBandBase) are stream variants
-constexpr int kBandBase = 400;     // variant ids >= kBandBase are band variants
+constexpr int kBandBase = 400;     // variant ids in [kBandBase, kHeadsBase) are band variants
+constexpr int kHeadsBase = 500;    // variant id kHeadsBase + v: the heads form of 16-bit forward row v
 
 // Row byte length from which the stream variants serve a row, per direction
 // (forward, backward).
@@ -124,6 +138,17 @@ constexpr bool same_shapes(const Variant* a, const Variant* b, int n)
 static_assert(count_of(kExFwdVec4) == count_of(kFwdVec4) && same_shapes(kExFwdVec4, kFwdVec4, count_of(kFwdVec4)) &&
                   count_of(kExFwdVec2) == count_of(kFwdVec2) && same_shapes(kExFwdVec2, kFwdVec2, count_of(kFwdVec2)),
               "explicit-mask forward rows must match the vector rows id for id");
+
+constexpr bool heads_rows_match()
+{
+    for (int i = 0; i < count_of(kFwdHeads2Ids); ++i) {
+        const Variant& v = kFwdVec2[kFwdHeads2Ids[i]];
+        if (v.team != kFwdHeads2[i].team || v.per_thread != kFwdHeads2[i].per_thread || v.team == 32)
+            return false;
+    }
+    return true;
+}
+static_assert(heads_rows_match(), "heads rows must match the 16-bit forward CTA-team rows they replace");
 
 // Variant table of the explicit-mask kernels (same ids as vec_table).
 inline VariantTable explicit_table(int direction, int elem_bytes)
@@ -169,6 +194,29 @@ inline int pick_variant(int direction, int64_t S, int elem_bytes, bool aligned16
     return -1;
 }
 
+inline VariantTable heads_table() { return VariantTable{kFwdHeads2, count_of(kFwdHeads2)}; }
+
+// The heads variant that replaces per-row vector variant `vec_id` of the 16-bit
+// forward, or -1.
+inline int heads_variant(int direction, int elem_bytes, int vec_id)
+{
+    if (direction != 0 || elem_bytes != 2)
+        return -1;
+    for (int i = 0; i < count_of(kFwdHeads2Ids); ++i)
+        if (kFwdHeads2Ids[i] == vec_id)
+            return kHeadsBase + vec_id;
+    return -1;
+}
+
+// Row of heads variant id (kHeadsBase + vector row id).
+inline Variant heads_row(int id)
+{
+    for (int i = 0; i < count_of(kFwdHeads2Ids); ++i)
+        if (kHeadsBase + kFwdHeads2Ids[i] == id)
+            return kFwdHeads2[i];
+    return kFwdHeads2[0];
+}
+
 inline VariantTable band_table(int direction)
 {
     return direction == 0 ? VariantTable{kFwdBand, count_of(kFwdBand)} : VariantTable{kBwdBand, count_of(kBwdBand)};
@@ -197,8 +245,20 @@ inline int pick_band_variant(int direction, int64_t S, int elem_bytes, bool alig
     return -1;
 }
 
+// Variant id that gtms_forward_masked / gtms_backward_masked launch for a
+// row-length choice: pick_variant, with the heads rows in place of the 16-bit
+// forward's CTA-team rows.
+inline int pick_launch_variant(int direction, int64_t S, int elem_bytes, bool aligned16)
+{
+    const int v = pick_variant(direction, S, elem_bytes, aligned16);
+    const int h = v >= 0 ? heads_variant(direction, elem_bytes, v) : -1;
+    return h >= 0 ? h : v;
+}
+
 inline Variant variant_at(int direction, int elem_bytes, int id)
 {
+    if (id >= kHeadsBase)
+        return heads_row(id);
     if (id >= kBandBase)
         return band_table(direction).rows[id - kBandBase];
     if (id >= kStreamBase)

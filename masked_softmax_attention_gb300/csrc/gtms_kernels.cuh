@@ -631,6 +631,54 @@ gtms_fwd_vec_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom
 }
 
 // ---------------------------------------------------------------------------
+// Heads forward: the vector forward with a team per (batch, row) pair that
+// runs the pair's M heads in turn. The heads share the row's kept range, so a
+// team loads head m + 1's kept units right after decoding head m's, and those
+// loads are in flight through head m's two reductions and its stores. Same
+// arithmetic in the same order as gtms_fwd_vec_kernel, so the same bits.
+// ---------------------------------------------------------------------------
+template <typename T, int MK, int TW, int NV, int MINB>
+__global__ void __launch_bounds__(TW == 32 ? kWarpTeamBlock : TW, MINB)
+gtms_fwd_heads_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom g, float scale)
+{
+    constexpr int EPU = 2 * Pairs<T>::kPairs;
+    __shared__ float red[TW > 32 ? 2 * (TW / 32) : 1];
+    float* red_max = red;
+    float* red_sum = TW > 32 ? red + TW / 32 : red;
+    const float c = __fmul_rn(scale, kLog2e);
+    const bool use_max = scale >= 0.0f;
+    int tid;
+    int64_t team, nteams;
+    team_coords<TW>(tid, team, nteams);
+    const auto unit_of = [tid](int k) { return tid + k * TW; };
+    const int32_t M = static_cast<int32_t>(g.rows_per_b / g.S);
+
+    for (int64_t qm = team; qm < g.rows / M; qm += nteams) {
+        const int32_t b = static_cast<int32_t>(qm / g.S), r = static_cast<int32_t>(qm % g.S);
+        int32_t c0, c1;
+        kept_range<MK>(seq_lens, b, r, g, c0, c1);
+        const UnitRange ur = UnitRange::of<EPU>(c0, c1);
+        const int64_t q0 = static_cast<int64_t>(b) * M * g.S + r;
+        Unit16 raw[NV];
+        load_kept<NV>(reinterpret_cast<const char*>(x + q0 * g.S), ur, unit_of, raw);
+        for (int32_t m = 0; m < M; ++m) {
+            const int64_t q = q0 + static_cast<int64_t>(m) * g.S;
+            char* yr = reinterpret_cast<char*>(y + q * g.S);
+            store_zeros<NV>(yr, ur, g.units, unit_of);
+            if (c1 <= c0)
+                continue;
+            float2 v[NV][Pairs<T>::kPairs];
+            float ext = fwd_decode_extreme<T, NV>(raw, v, ur, unit_of, use_max);
+            if (m + 1 < M)
+                load_kept<NV>(reinterpret_cast<const char*>(x + (q + g.S) * g.S), ur, unit_of, raw);
+            ext = use_max ? team_max<TW>(ext, red_max) : -team_max<TW>(-ext, red_max);
+            const float s = team_sum<TW>(fwd_exp_sum<T, NV>(v, ur, unit_of, ext, c), red_sum);
+            fwd_store<T, NV>(yr, v, ur, unit_of, __frcp_rn(s));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Vector backward: dx = scale * y * (dy - rowsum(dy * y)), one team per row.
 // The raw units of y and dy stay in registers; each pass decodes them.
 // ---------------------------------------------------------------------------

@@ -33,6 +33,14 @@ void launch_forward_mk(int id, const void* x, void* y, const int32_t* seq_lens, 
     case vid: gtms_fwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
 #define GTMS_FWD_ELEM_CASE(vid, tw, nv) \
     case kElemBase + vid: gtms_fwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
+#define GTMS_FWD_HEADS_CASE(vid, tw, nv, mb) \
+    case kHeadsBase + vid: gtms_fwd_heads_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows / (g.rows_per_b / g.S)), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
+    if constexpr (sizeof(T) == 2) {
+        switch (id) { GTMS_FWD_HEADS2(GTMS_FWD_HEADS_CASE) default: break; }
+        if (id >= kHeadsBase)
+            return;
+    }
+#undef GTMS_FWD_HEADS_CASE
 #define GTMS_FWD_BAND_CASE(vid, nv, mb) \
     case kBandBase + vid: gtms_fwd_band_kernel<T, nv, mb><<<grid_for<32>(g.rows), block_for<32>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
     if constexpr (MK == kMaskWindow) {

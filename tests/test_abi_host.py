@@ -79,13 +79,18 @@ def test_kernel_choice(lib):
     # vector kernels: a warp or a small CTA per row, sized by the row's 16-byte units
     assert gtms.kernel_name(0, 1000, F32) == "gtms_fwd_vec_kernel<f32,team64,x4,minb0>"
     assert gtms.kernel_name(1, 1000, F32) == "gtms_bwd_vec_kernel<f32,team32,x8,minb5>"
-    assert gtms.kernel_name(0, 2048, BF16) == "gtms_fwd_vec_kernel<bf16,team64,x4,minb16>"
+    assert gtms.kernel_name(0, 2048, BF16) == "gtms_fwd_heads_kernel<bf16,team64,x4,minb12>"
     assert gtms.kernel_name(1, 2048, BF16) == "gtms_bwd_vec_kernel<bf16,team32,x8,minb5>"
     assert gtms.kernel_name(1, 8192, F16) == "gtms_bwd_vec_kernel<f16,team128,x8,minb0>"
     assert gtms.kernel_name(0, 4096, F32) == "gtms_fwd_vec_kernel<f32,team256,x4,minb0>"
     assert gtms.kernel_name(0, 1024, F16) == "gtms_fwd_vec_kernel<f16,team32,x4,minb6>"
-    assert gtms.kernel_name(0, 8200, F16) == "gtms_fwd_vec_kernel<f16,team512,x4,minb2>"
-    assert gtms.kernel_name(0, 16376, BF16) == "gtms_fwd_vec_kernel<bf16,team512,x4,minb2>"   # 32752-byte rows
+    assert gtms.kernel_name(0, 8200, F16) == "gtms_fwd_heads_kernel<f16,team512,x4,minb1>"
+    assert gtms.kernel_name(0, 16376, BF16) == "gtms_fwd_heads_kernel<bf16,team512,x4,minb1>"   # 32752-byte rows
+    # 16-bit forwards of CTA-team rows: a team per (batch, row) pair runs its heads in turn
+    assert gtms.kernel_name(0, 8192, F16) == "gtms_fwd_heads_kernel<f16,team256,x4,minb3>"
+    assert gtms.kernel_name(0, 4096, BF16) == "gtms_fwd_heads_kernel<bf16,team128,x4,minb6>"
+    assert gtms.kernel_name(0, 1024, BF16) == "gtms_fwd_vec_kernel<bf16,team32,x4,minb6>"
+    assert gtms.kernel_name(1, 4096, BF16) == "gtms_bwd_vec_kernel<bf16,team64,x8,minb0>"
     # rows whose byte length is not a multiple of 16, or unaligned buffers: element kernels
     assert gtms.kernel_name(0, 5, F32) == "gtms_fwd_elem_kernel<f32,team32,x1>"
     assert gtms.kernel_name(0, 1000, F32, aligned16=False) == "gtms_fwd_elem_kernel<f32,team32,x32>"
@@ -102,7 +107,7 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name(0, 16384, F32, aligned16=False) == "none"
     # mask families: the row-length variant with the mask kind, or a warp-per-row band kernel for a
     # narrow sliding window in a row longer than one warp's 128 units
-    assert gtms.kernel_name_masked(0, 2048, BF16, 1) == "gtms_fwd_vec_kernel<bf16,team64,x4,minb16,mask1>"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 1) == "gtms_fwd_heads_kernel<bf16,team64,x4,minb12,mask1>"
     assert gtms.kernel_name_masked(0, 2048, BF16, 0) == gtms.kernel_name(0, 2048, BF16)
     assert gtms.kernel_name_masked(0, 2048, BF16, 2, 256) == "gtms_fwd_band_kernel<bf16,x2,minb8>"
     assert gtms.kernel_name_masked(1, 2048, BF16, 2, 256) == "gtms_bwd_band_kernel<bf16,x2,minb4>"
