@@ -2,7 +2,9 @@
 //
 // One "team" of threads owns one row of X[B,M,S,S] at a time: a warp for short
 // rows, a whole CTA for long ones (rows of 32 KB and more go to the two-pass
-// stream kernels of gtms_stream.cuh). The kept set of row r in batch b is a
+// stream kernels of gtms_stream.cuh; the 16-bit forward's CTA teams run the M
+// heads of one (batch, row) pair in turn, gtms_fwd_heads_kernel below; narrow
+// sliding windows go to the band kernels of gtms_band.cuh). The kept set of row r in batch b is a
 // contiguous column range [c0, c1) computed from (r, L_b, mask kind), with
 // L_b = clamp(seq_lens[b], 0, S). For the default op ("Attention-Mask-
 // Optimization" README, operator behaviour: kept iff r < L, c < L and c <= r)

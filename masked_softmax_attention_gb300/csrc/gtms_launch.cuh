@@ -29,8 +29,12 @@ void launch_forward_mk(int id, const void* x, void* y, const int32_t* seq_lens, 
 {
     const T* xp = static_cast<const T*>(x);
     T* yp = static_cast<T*>(y);
+// (16-bit CTA-team rows launch as heads kernels, so their per-row form is not instantiated.)
 #define GTMS_FWD_VEC_CASE(vid, tw, nv, mb) \
-    case vid: gtms_fwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
+    case vid: \
+        if constexpr (sizeof(T) == 4 || tw == 32) \
+            gtms_fwd_vec_kernel<T, MK, tw, nv, mb><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); \
+        break;
 #define GTMS_FWD_ELEM_CASE(vid, tw, nv) \
     case kElemBase + vid: gtms_fwd_elem_kernel<T, MK, tw, nv><<<grid_for<tw>(g.rows), block_for<tw>(), 0, st>>>(xp, yp, seq_lens, g, scale); break;
 #define GTMS_FWD_HEADS_CASE(vid, tw, nv, mb) \
