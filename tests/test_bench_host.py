@@ -1,0 +1,100 @@
+"""Host-side tests of bench.py (no GPU): the byte model, the traffic records and the
+reference arm's JSON line.
+
+The byte model is the roofline numerator, so it is checked against brute-force counts
+of the oracle's kept ranges and against the closed forms the definitions give.
+"""
+import dataclasses
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import bench
+import oracle
+import seeded_inputs as si
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _brute_kept(S, L, mask_kind, window):
+    """Kept elements of one slice, counted from the oracle's per-row kept ranges."""
+    c0, c1 = oracle.kept_ranges(np.array([L], dtype=np.int32), S, mask_kind, window)
+    return int(np.maximum(c1 - c0, 0).sum())
+
+
+@pytest.mark.parametrize("mask_kind,window", [(0, 0), (1, 0), (2, 1), (2, 7), (2, 64), (2, 1000)])
+def test_kept_per_slice_matches_brute_force(mask_kind, window):
+    S = 97
+    w = dataclasses.replace(si.custom("kept", 1, 1, S, "f32", 1.0, seq_lens=(S,)), mask_kind=mask_kind,
+                            window=window)
+    for L in (-3, 0, 1, 2, 13, 50, 96, 97, 120):
+        assert bench.kept_per_slice(w, L) == _brute_kept(S, L, mask_kind, window), (L, mask_kind, window)
+
+
+def test_required_bytes_closed_forms():
+    # the printed worked example: X[3,2,5,5] fp32, seq_lens 3, 4, 5 -> 4 * 2 * (6 + 10 + 15 + 3 * 25) bytes
+    w = si.WORKLOADS["worked_example"]
+    fwd, bwd = bench.required_bytes(w, si.seq_lens(w))
+    assert fwd == 848 and bwd == 0
+    # grouped tril, forward e * sum(live + S^2), backward e * sum(2 live + S^2)
+    w = si.custom("rb", 2, 3, 10, "bf16", 0.5, seq_lens=(4, 10))
+    live = 3 * (4 * 5 // 2 + 10 * 11 // 2)
+    assert bench.required_bytes(w, si.seq_lens(w)) == (2 * (live + 6 * 100), 2 * (2 * live + 6 * 100))
+    # an explicit mask counts its kept elements and its uint8 [B, S, S] bytes once
+    we = si.WORKLOADS["explicit_s2048_bf16"]
+    fb, bb = bench.required_bytes(we, si.seq_lens(we), kept_total=1000)
+    dense = we.B * we.M * we.S * we.S
+    assert fb == 2 * (1000 + dense) + we.B * we.S * we.S
+    assert bb == 2 * (2000 + dense) + we.B * we.S * we.S
+
+
+def test_traffic_records_are_keyed_by_kernel_workload_and_sources():
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    lines = [ln for ln in open(path, encoding="utf-8") if ln.startswith("traffic ")]
+    assert lines
+    for ln in lines:
+        kv = dict(tok.split("=", 1) for tok in ln.split()[1:])
+        got = bench.recorded_traffic(kv["kernel"], kv["workload"])
+        if kv["source_sha"] == bench.kernel_source_sha(kv["kernel"]):
+            assert got == int(kv["dram_bytes_per_launch"])
+        else:
+            assert got is None
+        # scaled from the stand-in by the ratio of algorithmic bytes, and within a few % of them
+        per = (int(kv["captured_read"]) + int(kv["captured_write"])) / int(kv["algorithmic_captured"])
+        assert 0.8 < per < 1.2
+    assert bench.recorded_traffic("gtms_no_such_kernel", "s1000_b12") is None
+
+
+def test_kernel_source_families_are_disjoint_but_share_the_common_header():
+    assert bench.attention_source("gtms_attn_tma.cuh") and bench.attention_source("gtms_tcgen05.cuh")
+    assert not bench.attention_source("gtms_kernels.cuh") and not bench.attention_source("gtms_stream.cuh")
+    assert bench.kernel_source_sha("gtms_attn_dscores_tma_kernel<bf16,d64>") != bench.kernel_source_sha(
+        "gtms_bwd_vec_kernel<f32,team32,x8,minb5>")
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "worked_example", "--steps", "1", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
+    assert d["config"]["workload"].startswith("worked_example")
+
+
+def test_fewer_than_three_warmup_steps_are_refused():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "worked_example", "--steps", "1", "--warmup", "2"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert out.returncode != 0
