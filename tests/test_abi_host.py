@@ -118,6 +118,12 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name_masked(0, 512, F32, 2, 7) == "gtms_fwd_vec_kernel<f32,team32,x4,minb8,mask2>"
     assert gtms.kernel_name_masked(0, 1000, F32, 2, 7, aligned16=False) == "gtms_fwd_elem_kernel<f32,team32,x32,mask2>"
     assert gtms.kernel_name_masked(0, 16384, F32, 2, 5000) == "gtms_fwd_stream_kernel<f32,team256,x4,minb4,mask2>"
+    # the band holds every run of w columns: (w + 2 * EPU - 2) // EPU units at most
+    assert gtms.kernel_name_masked(0, 2048, BF16, 2, 241) == "gtms_fwd_band_kernel<bf16,x1,minb8>"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 2, 250) == "gtms_fwd_band_kernel<bf16,x2,minb8>"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 2, 1017) == "gtms_fwd_band_kernel<bf16,x4,minb6>"
+    assert gtms.kernel_name_masked(0, 2048, BF16, 2, 1018) == "gtms_fwd_heads_kernel<bf16,team64,x4,minb12,mask2>"
+    assert gtms.kernel_name_masked(1, 2048, BF16, 2, 1018) == "gtms_bwd_vec_kernel<bf16,team32,x8,minb5,mask2>"
     assert gtms.kernel_name_masked(0, 2048, BF16, 2, 0) == "none"
     assert gtms.kernel_name_masked(0, 2048, BF16, 3, 1) == "none"
     # explicit-mask kernels: the vector rows, the forward with its own register caps, up to S = 8192

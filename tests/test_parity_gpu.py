@@ -445,6 +445,7 @@ MASK_CASES = [
     (2, 1, 1000, "f32"), (2, 7, 1000, "f32"), (2, 100, 2048, "bf16"), (2, 257, 33, "f16"), (2, 300, 8192, "f16"),
     (2, 5000, 16384, "f32"), (2, 8, 64, "bf16"), (2, 9, 5, "f32"),
     (2, 900, 4096, "bf16"), (2, 1500, 8192, "f16"), (2, 256, 2048, "bf16"),
+    (2, 1017, 2048, "bf16"),   # the widest window a 4-unit band lane set holds: 128 units at every offset
 ]
 
 
