@@ -114,22 +114,36 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def attention_source(name):
-    """Files the attention-backward kernels are compiled from (besides the shared gtms_kernels.cuh)."""
-    return name.startswith("gtms_attn") or name == "gtms_tcgen05.cuh"
+# Source files each kernel family is compiled from (csrc/), for the source hash that keys the
+# recorded DRAM traffic: a record stays valid while these files are unchanged.
+_COMMON_SOURCES = ("gtms_kernels.cuh", "gtms_dispatch.h", "gtms_launch.cuh")
+_FAMILY_SOURCES = (
+    ("gtms_attn", ("gtms_kernels.cuh", "gtms_tcgen05.cuh", "gtms_attn_bwd.cuh", "gtms_attn_tma.cuh",
+                   "gtms_attn_bwd.cu", "gtms_attn_tma.cu")),
+    ("gtms_fwd_explicit", _COMMON_SOURCES + ("gtms_explicit.cuh",)),
+    ("gtms_bwd_explicit", _COMMON_SOURCES + ("gtms_explicit.cuh",)),
+    ("gtms_fwd_stream", _COMMON_SOURCES + ("gtms_stream.cuh",)),
+    ("gtms_bwd_stream", _COMMON_SOURCES + ("gtms_stream.cuh",)),
+    ("gtms_fwd_band", _COMMON_SOURCES + ("gtms_band.cuh",)),
+    ("gtms_bwd_band", _COMMON_SOURCES + ("gtms_band.cuh",)),
+    ("gtms_fwd_staged", _COMMON_SOURCES + ("gtms_staged.cuh", "gtms_tcgen05.cuh")),
+)
+
+
+def kernel_sources(kernel):
+    """The csrc files a kernel (by its reported name) is compiled from."""
+    for prefix, files in _FAMILY_SOURCES:
+        if kernel.startswith(prefix):
+            return files
+    return _COMMON_SOURCES   # per-row vector, heads and element kernels
 
 
 def kernel_source_sha(kernel=""):
-    """Hash of the sources a kernel is compiled from: for the attention-backward
-    kernels their own files, for the softmax kernels every other file of csrc;
-    gtms_kernels.cuh belongs to both."""
-    import glob
-
-    attn = kernel.startswith("gtms_attn")
+    """Hash of the sources a kernel is compiled from (kernel_sources)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "masked_softmax_attention_gb300", "csrc", "*"))):
-        name = os.path.basename(p)
-        if name == "gtms_kernels.cuh" or attention_source(name) == attn:
+    for name in sorted(kernel_sources(kernel)):
+        p = os.path.join(ROOT, "masked_softmax_attention_gb300", "csrc", name)
+        if os.path.exists(p):
             with open(p, "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
@@ -269,33 +283,50 @@ def step_bytes(w, lens, kept_total=None):
 
 
 def oracle_step(ws, xb, dyb, threads):
-    """One oracle pass over the sample: forward, round, backward (all rows); for an
-    attention-backward sample, the dS step from (P, dO, V) and its rounding."""
+    """One oracle pass over the sample: forward, round, backward, round (all rows); for an
+    attention-backward sample, the dS step from (P, dO, V) and its rounding. With several
+    threads the rows are cut into chunks and each thread runs the whole pass (rounding
+    included) over its chunks, so no step runs on one core while the others wait."""
+    import concurrent.futures as cf
+
     import numpy as np
 
     import oracle
 
     lens = np.array(ws.fixed_seq_lens, dtype=np.int32)
-    if ws.head_dim > 0:
-        dout, v = dyb
-        ds = oracle.attn_dscores(xb, dout, v, lens, ws.B, ws.M, ws.S, ws.head_dim, ws.scale, ws.dtype_code,
-                                 threads=threads)
-        oracle.round_to(ds, ws.dtype_code)
-        return
-    if ws.keep_prob > 0:
-        dyb, mask = dyb
-        y = oracle.forward_explicit(xb, mask, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
-        yb = oracle.round_to(y, ws.dtype_code)
+    B, M, S, code = ws.B, ws.M, ws.S, ws.dtype_code
+    rows = B * M * S
+    x_rows = xb.reshape(-1)
+
+    def run(chunk):
+        r0, r1 = chunk
+        xs = x_rows[r0 * S:r1 * S]
+        if ws.head_dim > 0:
+            dout, v = dyb
+            oracle.round_to(oracle.attn_dscores(xs, dout, v, lens, B, M, S, ws.head_dim, ws.scale, code,
+                                                row_begin=r0, row_end=r1), code)
+            return
+        if ws.keep_prob > 0:
+            dy, mask = dyb
+            yb = oracle.round_to(oracle.forward_explicit(xs, mask, B, M, S, ws.scale, code, row_begin=r0,
+                                                         row_end=r1), code)
+            if ws.backward:
+                oracle.round_to(oracle.backward_explicit(yb, dy.reshape(-1)[r0 * S:r1 * S], mask, B, M, S,
+                                                         ws.scale, code, row_begin=r0, row_end=r1), code)
+            return
+        kw = dict(row_begin=r0, row_end=r1, mask_kind=ws.mask_kind, window=ws.window)
+        yb = oracle.round_to(oracle.forward(xs, lens, B, M, S, ws.scale, code, **kw), code)
         if ws.backward:
-            dx = oracle.backward_explicit(yb, dyb, mask, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, threads=threads)
-            oracle.round_to(dx, ws.dtype_code)
+            oracle.round_to(oracle.backward(yb, dyb.reshape(-1)[r0 * S:r1 * S], lens, B, M, S, ws.scale, code,
+                                            **kw), code)
+
+    if threads <= 1:
+        run((0, rows))
         return
-    kw = dict(threads=threads, mask_kind=ws.mask_kind, window=ws.window)
-    y = oracle.forward(xb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, **kw)
-    yb = oracle.round_to(y, ws.dtype_code)
-    if ws.backward:
-        dx = oracle.backward(yb, dyb, lens, ws.B, ws.M, ws.S, ws.scale, ws.dtype_code, **kw)
-        oracle.round_to(dx, ws.dtype_code)
+    step = -(-rows // (4 * threads))
+    chunks = [(r, min(r + step, rows)) for r in range(0, rows, step)]
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, chunks))
 
 
 def cpu_model():
@@ -391,6 +422,27 @@ def replica_workload(w, rank):
     import dataclasses
 
     return w if rank == 0 else dataclasses.replace(w, seed=w.seed + 1000 * rank)
+
+
+def shard_slices(n_slices, rank, world):
+    """Contiguous range [s0, s1) of the B*M (batch, head) slices that rank `rank` of `world`
+    runs when one workload is split over the ranks (sizes differ by at most one)."""
+    base, extra = divmod(n_slices, world)
+    s0 = rank * base + min(rank, extra)
+    return s0, s0 + base + (1 if rank < extra else 0)
+
+
+def shard_workload(w, lens, rank, world):
+    """Rank r's part of one workload split over `world` ranks: its range of (b, m) slices
+    as a [slices, 1, S, S] workload whose per-slice length is the slice's batch length
+    (the heads of a batch share it). Values come from the rank's own seeded draw with the
+    workload's distribution; the lengths, and so the bytes, are exactly the workload's."""
+    import dataclasses
+
+    s0, s1 = shard_slices(w.B * w.M, rank, world)
+    shard_lens = tuple(int(lens[s // w.M]) for s in range(s0, s1))
+    return dataclasses.replace(w, name=f"{w.name}_shard{rank}of{world}", B=s1 - s0, M=1, fixed_seq_lens=shard_lens,
+                               seq_len_range=None, seed=w.seed + 1000 * rank)
 
 
 def max_over_ranks(value, dist, device):
@@ -571,6 +623,121 @@ def run_e2e_attention_host_resident(args, w, lens, p, dout, v, stream, fn):
                             f"gtms_attn_dscores_kernel<{w.dtype},d{w.head_dim}>"}
 
 
+# Workloads timed one after another beside the headline step (rank 0 of a one-GPU
+# run): every listed configuration besides the headline one, the S = 4096 point,
+# the long rows, the other mask families, the explicit mask and the attention step.
+CONFIG_TABLE = ("worked_example", "s1000_b3", "s2048_bf16", "s8192_f16", "s4096_bf16", "s16384_bf16",
+                "s32768_bf16", "length_s2048_bf16", "window_s2048_bf16", "explicit_s2048_bf16",
+                "attn_s2048_bf16")
+L2_BYTES = 129 * 1000 * 1000
+
+
+def time_config(args, name, dev, stream, peak):
+    """Per-call CUDA-event timings of one workload through the C ABI: W untimed calls,
+    then K timed calls of the forward, then of the backward (or of the attention step),
+    inputs resident in HBM. Workloads whose tensors do not exceed L2 get an L2 flush
+    (a write of twice its size) before every timed call, outside the timed events.
+    Returns (entry, [(t0, t1) host windows of the timed loops])."""
+    import torch
+
+    import masked_softmax_attention_gb300 as gtms
+    import seeded_inputs as si
+
+    w = si.WORKLOADS[name]
+    lens = si.seq_lens(w)
+    lens_d = torch.from_numpy(lens).to(dev)
+    lib = gtms.load_library()
+    sp = stream.cuda_stream
+    keep = [lens_d]
+    calls = []
+    status = None
+    if w.head_dim > 0:
+        p = gtms.forward(si.make_x(w, dev), lens_d, w.scale)
+        dout, v = si.make_head_operands(w, dev)
+        ds = torch.empty_like(p)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        fn = lib.gtms_attention_softmax_backward
+        ca = (p.data_ptr(), dout.data_ptr(), v.data_ptr(), ds.data_ptr(), lens_d.data_ptr(), w.B, w.M, w.S,
+              w.head_dim, float(w.scale), w.dtype_code, status.data_ptr(), sp)
+        keep += [p, dout, v, ds, status]
+        calls.append(("attention_softmax_backward", lambda: fn(*ca), step_bytes(w, lens),
+                      f"gtms_attn_dscores_tma_kernel<{w.dtype},d{w.head_dim}>"))
+        tensor_bytes = p.numel() * p.element_size()
+    else:
+        x = si.make_x(w, dev)
+        y = torch.empty_like(x)
+        mask = si.make_keep_mask(w, dev) if w.keep_prob > 0 else None
+        kept_total = int(torch.count_nonzero(mask).item()) * w.M if mask is not None else None
+        fwd_c, bwd_c, _, _ = entry_points(lib, w)
+        fb, bb = required_bytes(w, lens, kept_total)
+        xp, yp, lp = x.data_ptr(), y.data_ptr(), lens_d.data_ptr()
+        mp = mask.data_ptr() if mask is not None else None
+        keep += [x, y, mask]
+        calls.append(("forward", lambda: fwd_c(xp, yp, lp, mp, sp), fb, kernel_label(gtms, w, 0)))
+        if w.backward:
+            dy = si.make_dy(w, dev)
+            dx = torch.empty_like(x)
+            dyp, dxp = dy.data_ptr(), dx.data_ptr()
+            keep += [dy, dx]
+            calls.append(("backward", lambda: bwd_c(yp, dyp, dxp, lp, mp, sp), bb, kernel_label(gtms, w, 1)))
+        tensor_bytes = x.numel() * x.element_size()
+    flush = None
+    if tensor_bytes <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    entry = {"workload": w.name + ": " + w.describe()}
+    windows = []
+    for label, call, nbytes, kname in calls:
+        for _ in range(args.warmup):
+            if call():
+                raise RuntimeError(f"{name} {label}: libgtms call failed")
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        t0 = time.time()
+        rc = 0
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                if flush is not None:
+                    flush.zero_()
+                a.record(stream)
+                rc |= call()
+                b.record(stream)
+        torch.cuda.synchronize()
+        windows.append((t0, time.time()))
+        if rc:
+            raise RuntimeError(f"{name} {label}: libgtms call failed inside the timed loop")
+        ms = [a.elapsed_time(b) for a, b in ev]
+        mean = statistics.fmean(ms)
+        gbs = nbytes / (mean * 1e-3) / 1e9
+        entry[label] = {"kernel": kname, "ms_per_call": round(mean, 5),
+                        "ms_median": round(statistics.median(ms), 5), "ms_min": round(min(ms), 5),
+                        "required_bytes": nbytes, "achieved_gbs": round(gbs, 2),
+                        "frac_of_peak": round(gbs / peak, 4)}
+        if flush is not None:
+            entry[label]["l2"] = "flushed before every timed call (tensors smaller than L2); latency only"
+    if status is not None and int(status.item()):
+        raise RuntimeError(f"{name}: a bounded wait inside the attention kernel ran out")
+    del keep, calls, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return entry, windows
+
+
+def time_configs(args, dev, stream, peak, sampler):
+    """The CONFIG_TABLE workloads (or --configs), one after another, buffers freed between them."""
+    names = CONFIG_TABLE if args.configs is None else [n for n in args.configs.split(",") if n]
+    out, windows = {}, []
+    for name in names:
+        entry, win = time_config(args, name, dev, stream, peak)
+        out[name] = entry
+        windows += win
+    if sampler is not None and windows:
+        out["clocks"] = sampler.summary(min(t for t, _ in windows), max(t for _, t in windows))
+    out["timing"] = (f"CUDA events around each call on the launching stream; {args.warmup} untimed then "
+                     f"{args.steps} timed calls per direction; ms_per_call is the mean")
+    return out
+
+
 def run_gpu(args, w, lens, rank, world, local_rank):
     import torch
 
@@ -588,7 +755,9 @@ def run_gpu(args, w, lens, rank, world, local_rank):
 
         dist.init_process_group("nccl", device_id=dev)
 
-    wr = replica_workload(w, rank)
+    if args.split and (w.keep_prob > 0 or w.head_dim > 0):
+        raise SystemExit("--split serves the mask-family workloads (seq_lens masks) only")
+    wr = shard_workload(w, lens, rank, world) if args.split else replica_workload(w, rank)
     lens_r = si.seq_lens(wr)
     x = si.make_x(wr, dev)
     dy = si.make_dy(wr, dev)
@@ -665,6 +834,10 @@ def run_gpu(args, w, lens, rank, world, local_rank):
                 "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json hbm_gbs' if peak_kind == 'measured' else 'recipe fallback 6.8 TB/s'})",
                 "algorithmic_bytes_per_launch": dk["required_bytes"]}
 
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = time_configs(args, dev, stream, peak, sampler)
+
     e2e = e2e_staged = None
     if args.e2e_steps > 0:
         e2e = run_e2e_host_resident(args, wr, lens_r, dev, stream, fwd_c, bwd_c, mask, kept_total)
@@ -677,12 +850,17 @@ def run_gpu(args, w, lens, rank, world, local_rank):
         sampler.stop()
 
     if rank == 0:
+        config = workload_config(w, lens, kept_total) if args.split else workload_config(wr, lens_r, kept_total)
+        if args.split:
+            config["parallelism"] = (f"one workload split over {world} GPU(s): rank r runs a contiguous range of "
+                                     "the B*M (batch, head) slices, no collective on the data path")
         line = {"metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-                "config": workload_config(wr, lens_r, kept_total), "pct_hbm_peak": round(100 * (value / world) / peak, 2),
+                "scaling": "strong" if args.split else "weak", "vs_baseline": None, "dtype": w.dtype,
+                "data": "synthetic", "config": config, "pct_hbm_peak": round(100 * (value / world) / peak, 2),
                 "ms_per_step_median": round(statistics.median(step_ms), 5), "ms_per_step_min": round(min(step_ms), 5),
-                "kernels": kern, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "e2e_staged": e2e_staged,
+                "kernels": kern, "roofline": roofline, "configs": configs, "cpu_baseline": cpu, "e2e": e2e,
+                "e2e_staged": e2e_staged,
                 "gpu_launches": K * (2 if wr.backward else 1), "clocks": clocks,
                 "impl": "gtms"}
         print(json.dumps(line), flush=True)
@@ -803,6 +981,10 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunk", type=int, default=1, help="batches per chunk in the host pipeline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table (CONFIG_TABLE)")
+    ap.add_argument("--split", action="store_true",
+                    help="split one workload over the ranks (strong scaling) instead of one replica per rank")
+    ap.add_argument("--configs", default=None, help="comma-separated workloads for the per-workload table")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -1,9 +1,10 @@
 """The N > 1 host logic of bench.py on CPU: two gloo ranks, no GPU.
 
-Rows are independent, so each rank runs its own replica of the workload with
-no data-path collective; the only exchange is the max over ranks of the step
-time. These tests run that exchange and the whole-job value under a real
-two-process gloo group.
+Rows are independent, so each rank runs either its own replica of the workload
+(weak scaling) or a contiguous range of one workload's (batch, head) slices
+(--split, strong scaling), with no data-path collective; the only exchanges are
+the max over ranks of the step time and the sum of the bytes moved. These tests
+run those exchanges and the whole-job value under a real two-process gloo group.
 """
 import os
 import socket
@@ -59,3 +60,47 @@ def test_single_rank_needs_no_group():
     assert bench.sum_over_ranks(7.0, None, torch.device("cpu")) == 7.0
     w = si.WORKLOADS["s1000_b12"]
     assert bench.replica_workload(w, 0) is w
+
+
+def _split_rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = si.WORKLOADS["s1000_b12"]
+        lens = si.seq_lens(w)
+        ws = bench.shard_workload(w, lens, rank, world)
+        fb, bb = bench.required_bytes(ws, si.seq_lens(ws))
+        total = bench.sum_over_ranks(fb + bb, dist, torch.device("cpu"))
+        out[rank] = (bench.shard_slices(w.B * w.M, rank, world), ws.B, ws.M, tuple(si.seq_lens(ws)), total)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_split_one_workload_exactly():
+    world, port = 2, _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.start_processes(_split_rank_main, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+        res = dict(out)
+    w = si.WORKLOADS["s1000_b12"]
+    lens = si.seq_lens(w)
+    (r0, b0, m0, l0, t0), (r1, b1, m1, l1, t1) = res[0], res[1]
+    # the two ranges tile the B*M slices, each slice once, and carry its batch's length
+    assert r0 == (0, w.B * w.M // 2) and r1 == (w.B * w.M // 2, w.B * w.M)
+    assert (b0, m0, b1, m1) == (r0[1] - r0[0], 1, r1[1] - r1[0], 1)
+    assert l0 + l1 == tuple(int(lens[s // w.M]) for s in range(w.B * w.M))
+    # the whole job moves exactly the bytes of the unsplit workload
+    fb, bb = bench.required_bytes(w, lens)
+    assert t0 == t1 == fb + bb
+
+
+@pytest.mark.parametrize("n", [0, 1, 5, 12, 768, 1001])
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_shard_slices_tile_the_slices(n, world):
+    ranges = [bench.shard_slices(n, r, world) for r in range(world)]
+    assert ranges[0][0] == 0 and ranges[-1][1] == n
+    for (a0, a1), (b0, b1) in zip(ranges, ranges[1:]):
+        assert a1 == b0
+    sizes = [b - a for a, b in ranges]
+    assert max(sizes) - min(sizes) <= 1 and min(sizes) >= 0
