@@ -45,7 +45,14 @@
  *                        whose byte length is not a multiple of 16 or a buffer
  *                        that is not 16-byte aligned (long rows are streamed
  *                        in 16-byte units only).
- *   GTMS_ERR_CUDA        the kernel launch failed (cudaGetLastError()).
+ *   GTMS_ERR_CUDA        the kernel launch failed (the status the launch call
+ *                        itself returned; an error left behind by earlier,
+ *                        unrelated work on the thread is not reported here).
+ *   GTMS_ERR_TIMEOUT     never returned by a call, which returns before its
+ *                        kernel runs: it is the code that the attention step's
+ *                        kernel writes into the caller's status word when one of
+ *                        its bounded internal waits ran out (see
+ *                        gtms_attention_softmax_backward).
  * All argument checks run on the host before anything is enqueued; a call
  * that returns an error has enqueued nothing.
  */
@@ -83,7 +90,8 @@ typedef enum {
     GTMS_OK = 0,
     GTMS_ERR_INVALID_ARG = 1,
     GTMS_ERR_UNSUPPORTED = 2,
-    GTMS_ERR_CUDA = 3
+    GTMS_ERR_CUDA = 3,
+    GTMS_ERR_TIMEOUT = 4
 } gtms_status;
 
 /*
@@ -181,9 +189,12 @@ int gtms_backward_explicit(const void* y, const void* dy, void* dx, const uint8_
  * kept entry.
  *   seq_lens device int32[B]; scale finite.
  *   head_dim 64 or 128; dtype GTMS_BF16 or GTMS_F16; S a multiple of 8.
- *   status   NULL, or a device int32 the kernel ORs 1 into if one of its
- *            bounded internal waits ran out (the caller clears it); results
- *            are then incomplete.
+ *   status   NULL, or a device-addressable int32 that the kernel ORs
+ *            GTMS_ERR_TIMEOUT into when one of its internal waits (a hand-off
+ *            between its warps, each bounded to 1 s of GPU time) ran out; the
+ *            kernel then stops early and its results are incomplete. The
+ *            caller clears the word before the call and reads it after
+ *            synchronising with `stream`: 0, or GTMS_ERR_TIMEOUT.
  * All pointers 16-byte aligned (status 4-byte). GTMS_ERR_UNSUPPORTED: fp32,
  * other head dims, S not a multiple of 8, S > GTMS_MAX_S. Otherwise as
  * gtms_backward.

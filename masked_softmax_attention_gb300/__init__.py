@@ -22,7 +22,7 @@ import threading
 from ._build import LIB_PATH, build_library  # noqa: F401  (re-exported for build scripts)
 
 GTMS_F32, GTMS_BF16, GTMS_F16 = 0, 1, 2
-GTMS_OK, GTMS_ERR_INVALID_ARG, GTMS_ERR_UNSUPPORTED, GTMS_ERR_CUDA = 0, 1, 2, 3
+GTMS_OK, GTMS_ERR_INVALID_ARG, GTMS_ERR_UNSUPPORTED, GTMS_ERR_CUDA, GTMS_ERR_TIMEOUT = 0, 1, 2, 3, 4
 GTMS_MAX_S = 65536
 GTMS_MASK_GROUPED_TRIL, GTMS_MASK_LENGTH, GTMS_MASK_SLIDING_WINDOW = 0, 1, 2
 

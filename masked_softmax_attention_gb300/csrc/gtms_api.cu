@@ -17,14 +17,15 @@
 
 namespace gtms {
 template <typename T, int MK>
-void launch_forward(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+cudaError_t launch_forward(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
 template <typename T, int MK>
-void launch_backward(int, const void*, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+cudaError_t launch_backward(int, const void*, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
 // Instantiated one per translation unit (gtms_{fwd,bwd}_<dtype>_<mask>.cu).
 #define GTMS_EXTERN_FOR(T, MK) \
-    extern template void launch_forward<T, MK>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t); \
-    extern template void launch_backward<T, MK>(int, const void*, const void*, void*, const int32_t*, const Geom&, float, \
-                                                cudaStream_t);
+    extern template cudaError_t launch_forward<T, MK>(int, const void*, void*, const int32_t*, const Geom&, float,   \
+                                                      cudaStream_t);                                               \
+    extern template cudaError_t launch_backward<T, MK>(int, const void*, const void*, void*, const int32_t*,        \
+                                                       const Geom&, float, cudaStream_t);
 GTMS_EXTERN_FOR(float, 0)
 GTMS_EXTERN_FOR(float, 1)
 GTMS_EXTERN_FOR(float, 2)
@@ -36,41 +37,41 @@ GTMS_EXTERN_FOR(__half, 1)
 GTMS_EXTERN_FOR(__half, 2)
 #undef GTMS_EXTERN_FOR
 template <typename T>
-void launch_forward_explicit(int, const void*, void*, const uint8_t*, int32_t, const Geom&, float, cudaStream_t);
+cudaError_t launch_forward_explicit(int, const void*, void*, const uint8_t*, int32_t, const Geom&, float, cudaStream_t);
 template <typename T>
-void launch_backward_explicit(int, const void*, const void*, void*, const uint8_t*, int32_t, const Geom&, float,
-                              cudaStream_t);
+cudaError_t launch_backward_explicit(int, const void*, const void*, void*, const uint8_t*, int32_t, const Geom&, float,
+                                     cudaStream_t);
 #define GTMS_EXTERN_EXPLICIT(T)                                                                                     \
-    extern template void launch_forward_explicit<T>(int, const void*, void*, const uint8_t*, int32_t, const Geom&, \
-                                                    float, cudaStream_t);                                          \
-    extern template void launch_backward_explicit<T>(int, const void*, const void*, void*, const uint8_t*, int32_t, \
-                                                     const Geom&, float, cudaStream_t);
+    extern template cudaError_t launch_forward_explicit<T>(int, const void*, void*, const uint8_t*, int32_t,        \
+                                                           const Geom&, float, cudaStream_t);                      \
+    extern template cudaError_t launch_backward_explicit<T>(int, const void*, const void*, void*, const uint8_t*,   \
+                                                            int32_t, const Geom&, float, cudaStream_t);
 GTMS_EXTERN_EXPLICIT(float)
 GTMS_EXTERN_EXPLICIT(__nv_bfloat16)
 GTMS_EXTERN_EXPLICIT(__half)
 #undef GTMS_EXTERN_EXPLICIT
 template <typename T, int D>
 cudaError_t launch_attn_dscores(const void*, const void*, const void*, void*, const int32_t*, int64_t, int64_t,
-                                int64_t, float, int32_t*, cudaStream_t);
+                                int64_t, float, int32_t*, cudaStream_t, uint64_t);
 extern template cudaError_t launch_attn_dscores<__nv_bfloat16, 64>(const void*, const void*, const void*, void*,
                                                                    const int32_t*, int64_t, int64_t, int64_t, float,
-                                                                   int32_t*, cudaStream_t);
+                                                                   int32_t*, cudaStream_t, uint64_t);
 extern template cudaError_t launch_attn_dscores<__nv_bfloat16, 128>(const void*, const void*, const void*, void*,
                                                                     const int32_t*, int64_t, int64_t, int64_t, float,
-                                                                    int32_t*, cudaStream_t);
+                                                                    int32_t*, cudaStream_t, uint64_t);
 extern template cudaError_t launch_attn_dscores<__half, 64>(const void*, const void*, const void*, void*,
                                                             const int32_t*, int64_t, int64_t, int64_t, float,
-                                                            int32_t*, cudaStream_t);
+                                                            int32_t*, cudaStream_t, uint64_t);
 extern template cudaError_t launch_attn_dscores<__half, 128>(const void*, const void*, const void*, void*,
                                                              const int32_t*, int64_t, int64_t, int64_t, float,
-                                                             int32_t*, cudaStream_t);
+                                                             int32_t*, cudaStream_t, uint64_t);
 template <typename T, int D>
 cudaError_t launch_attn_dscores_tma(const void*, const void*, const void*, void*, const int32_t*, int64_t, int64_t,
-                                    int64_t, float, int32_t*, cudaStream_t);
+                                    int64_t, float, int32_t*, cudaStream_t, uint64_t);
 #define GTMS_EXTERN_ATTN_TMA(T, D)                                                                              \
     extern template cudaError_t launch_attn_dscores_tma<T, D>(const void*, const void*, const void*, void*,     \
                                                               const int32_t*, int64_t, int64_t, int64_t, float, \
-                                                              int32_t*, cudaStream_t);
+                                                              int32_t*, cudaStream_t, uint64_t);
 GTMS_EXTERN_ATTN_TMA(__nv_bfloat16, 64)
 GTMS_EXTERN_ATTN_TMA(__nv_bfloat16, 128)
 GTMS_EXTERN_ATTN_TMA(__half, 64)
@@ -171,30 +172,36 @@ int check_mask(int mask_kind, int64_t window)
 }
 
 template <typename T>
-void run_forward(int kind, int variant, const void* x, void* y, const int32_t* seq_lens, const gtms::Geom& g,
-                 float scale, cudaStream_t st)
+cudaError_t run_forward(int kind, int variant, const void* x, void* y, const int32_t* seq_lens, const gtms::Geom& g,
+                        float scale, cudaStream_t st)
 {
     switch (kind) {
-    case 0: gtms::launch_forward<T, 0>(variant, x, y, seq_lens, g, scale, st); break;
-    case 1: gtms::launch_forward<T, 1>(variant, x, y, seq_lens, g, scale, st); break;
-    default: gtms::launch_forward<T, 2>(variant, x, y, seq_lens, g, scale, st); break;
+    case 0: return gtms::launch_forward<T, 0>(variant, x, y, seq_lens, g, scale, st);
+    case 1: return gtms::launch_forward<T, 1>(variant, x, y, seq_lens, g, scale, st);
+    default: return gtms::launch_forward<T, 2>(variant, x, y, seq_lens, g, scale, st);
     }
 }
 
 template <typename T>
-void run_backward(int kind, int variant, const void* y, const void* dy, void* dx, const int32_t* seq_lens,
-                  const gtms::Geom& g, float scale, cudaStream_t st)
+cudaError_t run_backward(int kind, int variant, const void* y, const void* dy, void* dx, const int32_t* seq_lens,
+                         const gtms::Geom& g, float scale, cudaStream_t st)
 {
     switch (kind) {
-    case 0: gtms::launch_backward<T, 0>(variant, y, dy, dx, seq_lens, g, scale, st); break;
-    case 1: gtms::launch_backward<T, 1>(variant, y, dy, dx, seq_lens, g, scale, st); break;
-    default: gtms::launch_backward<T, 2>(variant, y, dy, dx, seq_lens, g, scale, st); break;
+    case 0: return gtms::launch_backward<T, 0>(variant, y, dy, dx, seq_lens, g, scale, st);
+    case 1: return gtms::launch_backward<T, 1>(variant, y, dy, dx, seq_lens, g, scale, st);
+    default: return gtms::launch_backward<T, 2>(variant, y, dy, dx, seq_lens, g, scale, st);
     }
 }
 
-int launch_status()
+// Status of a launch from the launch call's own return value. A failed launch
+// also leaves its error as the thread's last error, which is cleared here: it
+// has been reported through the returned code.
+int launch_status(cudaError_t e)
 {
-    return cudaGetLastError() == cudaSuccess ? GTMS_OK : GTMS_ERR_CUDA;
+    if (e == cudaSuccess)
+        return GTMS_OK;
+    cudaGetLastError();
+    return GTMS_ERR_CUDA;
 }
 
 }  // namespace
@@ -225,11 +232,10 @@ GTMS_EXPORT int gtms_forward_masked(const void* x, void* y, const int32_t* seq_l
     const gtms::Geom g = make_geom(0, c.rows, M, S, variant, e, window);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
-    case GTMS_F32: run_forward<float>(mask_kind, variant, x, y, seq_lens, g, scale, st); break;
-    case GTMS_BF16: run_forward<__nv_bfloat16>(mask_kind, variant, x, y, seq_lens, g, scale, st); break;
-    default: run_forward<__half>(mask_kind, variant, x, y, seq_lens, g, scale, st); break;
+    case GTMS_F32: return launch_status(run_forward<float>(mask_kind, variant, x, y, seq_lens, g, scale, st));
+    case GTMS_BF16: return launch_status(run_forward<__nv_bfloat16>(mask_kind, variant, x, y, seq_lens, g, scale, st));
+    default: return launch_status(run_forward<__half>(mask_kind, variant, x, y, seq_lens, g, scale, st));
     }
-    return launch_status();
 }
 
 GTMS_EXPORT int gtms_forward(const void* x, void* y, const int32_t* seq_lens, int64_t B, int64_t M, int64_t S,
@@ -265,11 +271,11 @@ GTMS_EXPORT int gtms_backward_masked(const void* y, const void* dy, void* dx, co
     const gtms::Geom g = make_geom(1, c.rows, M, S, variant, e, window);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
-    case GTMS_F32: run_backward<float>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st); break;
-    case GTMS_BF16: run_backward<__nv_bfloat16>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st); break;
-    default: run_backward<__half>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st); break;
+    case GTMS_F32: return launch_status(run_backward<float>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st));
+    case GTMS_BF16:
+        return launch_status(run_backward<__nv_bfloat16>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st));
+    default: return launch_status(run_backward<__half>(mask_kind, variant, y, dy, dx, seq_lens, g, scale, st));
     }
-    return launch_status();
 }
 
 GTMS_EXPORT int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B, int64_t M,
@@ -313,11 +319,11 @@ GTMS_EXPORT int gtms_forward_explicit(const void* x, void* y, const uint8_t* mas
     const int32_t mb = static_cast<int32_t>(mask_batches);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
-    case GTMS_F32: gtms::launch_forward_explicit<float>(variant, x, y, mask, mb, g, scale, st); break;
-    case GTMS_BF16: gtms::launch_forward_explicit<__nv_bfloat16>(variant, x, y, mask, mb, g, scale, st); break;
-    default: gtms::launch_forward_explicit<__half>(variant, x, y, mask, mb, g, scale, st); break;
+    case GTMS_F32: return launch_status(gtms::launch_forward_explicit<float>(variant, x, y, mask, mb, g, scale, st));
+    case GTMS_BF16:
+        return launch_status(gtms::launch_forward_explicit<__nv_bfloat16>(variant, x, y, mask, mb, g, scale, st));
+    default: return launch_status(gtms::launch_forward_explicit<__half>(variant, x, y, mask, mb, g, scale, st));
     }
-    return launch_status();
 }
 
 GTMS_EXPORT int gtms_backward_explicit(const void* y, const void* dy, void* dx, const uint8_t* mask,
@@ -340,11 +346,11 @@ GTMS_EXPORT int gtms_backward_explicit(const void* y, const void* dy, void* dx, 
     const int32_t mb = static_cast<int32_t>(mask_batches);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     switch (dtype) {
-    case GTMS_F32: gtms::launch_backward_explicit<float>(variant, y, dy, dx, mask, mb, g, scale, st); break;
-    case GTMS_BF16: gtms::launch_backward_explicit<__nv_bfloat16>(variant, y, dy, dx, mask, mb, g, scale, st); break;
-    default: gtms::launch_backward_explicit<__half>(variant, y, dy, dx, mask, mb, g, scale, st); break;
+    case GTMS_F32: return launch_status(gtms::launch_backward_explicit<float>(variant, y, dy, dx, mask, mb, g, scale, st));
+    case GTMS_BF16:
+        return launch_status(gtms::launch_backward_explicit<__nv_bfloat16>(variant, y, dy, dx, mask, mb, g, scale, st));
+    default: return launch_status(gtms::launch_backward_explicit<__half>(variant, y, dy, dx, mask, mb, g, scale, st));
     }
-    return launch_status();
 }
 
 GTMS_EXPORT int gtms_attention_softmax_backward(const void* p, const void* dout, const void* v, void* ds,
@@ -380,18 +386,18 @@ GTMS_EXPORT int gtms_attention_softmax_backward(const void* p, const void* dout,
     cudaError_t e;
     if (dtype == GTMS_BF16) {
         if (tma)
-            e = head_dim == 64 ? gtms::launch_attn_dscores_tma<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
-                               : gtms::launch_attn_dscores_tma<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+            e = head_dim == 64 ? gtms::launch_attn_dscores_tma<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs)
+                               : gtms::launch_attn_dscores_tma<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs);
         else
-            e = head_dim == 64 ? gtms::launch_attn_dscores<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
-                               : gtms::launch_attn_dscores<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+            e = head_dim == 64 ? gtms::launch_attn_dscores<__nv_bfloat16, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs)
+                               : gtms::launch_attn_dscores<__nv_bfloat16, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs);
     } else {
         if (tma)
-            e = head_dim == 64 ? gtms::launch_attn_dscores_tma<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
-                               : gtms::launch_attn_dscores_tma<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+            e = head_dim == 64 ? gtms::launch_attn_dscores_tma<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs)
+                               : gtms::launch_attn_dscores_tma<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs);
         else
-            e = head_dim == 64 ? gtms::launch_attn_dscores<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st)
-                               : gtms::launch_attn_dscores<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st);
+            e = head_dim == 64 ? gtms::launch_attn_dscores<__half, 64>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs)
+                               : gtms::launch_attn_dscores<__half, 128>(p, dout, v, ds, seq_lens, B, M, S, scale, status, st, gtms::kAttnWaitNs);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -425,6 +431,7 @@ GTMS_EXPORT const char* gtms_status_string(int status)
     case GTMS_ERR_INVALID_ARG: return "GTMS_ERR_INVALID_ARG";
     case GTMS_ERR_UNSUPPORTED: return "GTMS_ERR_UNSUPPORTED";
     case GTMS_ERR_CUDA: return "GTMS_ERR_CUDA";
+    case GTMS_ERR_TIMEOUT: return "GTMS_ERR_TIMEOUT";
     default: return "GTMS_UNKNOWN_STATUS";
     }
 }

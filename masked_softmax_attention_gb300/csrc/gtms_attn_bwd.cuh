@@ -32,14 +32,15 @@
 // that are contiguous along each row.
 //
 // Only 16-byte units of P that hold a kept element are fetched. Every wait on
-// the MMA's mbarrier is bounded; if one runs out the kernel ORs 1 into the
-// caller's status word, skips the remaining work, frees its tensor memory and
-// returns.
+// the MMA's mbarrier is bounded in time; if one runs out the kernel ORs
+// GTMS_ERR_TIMEOUT into the caller's status word, skips the remaining work,
+// frees its tensor memory and returns.
 #pragma once
 
 #include <cstdint>
 #include <type_traits>
 
+#include "gtms.h"
 #include "gtms_kernels.cuh"
 #include "gtms_tcgen05.cuh"
 
@@ -47,7 +48,6 @@ namespace gtms {
 
 constexpr int kAttnRows = 128;      // rows per CTA (the MMA's M) and columns per tile (its N)
 constexpr int kAttnThreads = 256;
-constexpr int kAttnWaitLimit = 1 << 24;
 constexpr uint32_t kAttnPTileBytes = kAttnRows * 256;   // one 128 x 128 tile of 16-bit P or dS
 
 template <int D>
@@ -171,7 +171,8 @@ __device__ __forceinline__ void zero_region(T* slice, int32_t S, int32_t row0, i
 template <typename T, int D>
 __global__ void __launch_bounds__(kAttnThreads, 2)
 gtms_attn_dscores_kernel(const T* P, const T* dO, const T* V, T* dS, const int32_t* __restrict__ seq_lens,
-                         int32_t M, int32_t S, int32_t n_row_blocks, float scale, int32_t* status)
+                         int32_t M, int32_t S, int32_t n_row_blocks, float scale, int32_t* status,
+                         uint64_t wait_ns)
 {
     using IO = Pairs<T>;
     using SM = AttnSmem<D>;
@@ -259,7 +260,7 @@ gtms_attn_dscores_kernel(const T* P, const T* dO, const T* V, T* dS, const int32
             fetch_p_tile<T>(nx_v + SM::op, tl, p_slice, S, r0, L, tn);
             tc::cp_async_commit();
         }
-        const bool ok = tc::mbar_wait(&mbar, phase, kAttnWaitLimit);
+        const bool ok = tc::mbar_wait(&mbar, phase, wait_ns);
         phase ^= 1u;
         if (__syncthreads_or(!ok)) {
             failed = true;
@@ -350,8 +351,8 @@ gtms_attn_dscores_kernel(const T* P, const T* dO, const T* V, T* dS, const int32
     tc::cp_async_wait_all();
     if (failed) {
         if (tid == 0 && status)
-            atomicOr(status, 1);
-        tc::mbar_wait(&mbar, phase ^ 1u, kAttnWaitLimit);   // one more bounded wait for the MMA in flight
+            atomicOr(status, GTMS_ERR_TIMEOUT);
+        tc::mbar_wait(&mbar, phase ^ 1u, kAttnDrainWaitNs);   // one more bounded wait for the MMA in flight
         tc::fence_before_sync();
         __syncthreads();
     }
@@ -363,7 +364,8 @@ gtms_attn_dscores_kernel(const T* P, const T* dO, const T* V, T* dS, const int32
 // holds dO and two stages of (V tile, P tile).
 template <typename T, int D>
 cudaError_t launch_attn_dscores(const void* P, const void* dO, const void* V, void* dS, const int32_t* seq_lens,
-                                int64_t B, int64_t M, int64_t S, float scale, int32_t* status, cudaStream_t st)
+                                int64_t B, int64_t M, int64_t S, float scale, int32_t* status, cudaStream_t st,
+                                uint64_t wait_ns = kAttnWaitNs)
 {
     constexpr int smem = static_cast<int>(AttnSmem<D>::total);
     auto* kern = gtms_attn_dscores_kernel<T, D>;
@@ -372,10 +374,9 @@ cudaError_t launch_attn_dscores(const void* P, const void* dO, const void* V, vo
         return e;
     const int32_t nrb = static_cast<int32_t>((S + kAttnRows - 1) / kAttnRows);
     const int64_t grid = B * M * nrb;
-    kern<<<static_cast<unsigned>(grid), kAttnThreads, smem, st>>>(
-        static_cast<const T*>(P), static_cast<const T*>(dO), static_cast<const T*>(V), static_cast<T*>(dS), seq_lens,
-        static_cast<int32_t>(M), static_cast<int32_t>(S), nrb, scale, status);
-    return cudaGetLastError();
+    return launch_kernel(kern, static_cast<unsigned>(grid), kAttnThreads, smem, st, static_cast<const T*>(P),
+                         static_cast<const T*>(dO), static_cast<const T*>(V), static_cast<T*>(dS), seq_lens,
+                         static_cast<int32_t>(M), static_cast<int32_t>(S), nrb, scale, status, wait_ns);
 }
 
 }  // namespace gtms

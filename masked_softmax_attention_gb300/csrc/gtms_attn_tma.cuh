@@ -26,10 +26,11 @@
 //                      are dropped by the TMA unit) and returns the stage;
 //   zero (2 warps)     zero-fill each block's columns right of the diagonal
 //                      tile, and whole padded row blocks.
-// Every hand-off is an mbarrier; every wait is bounded. If a wait runs out, the
-// kernel ORs 1 into the caller's status word, every role leaves its loop, the
-// outstanding copies and MMAs are waited for (bounded) and the tensor memory is
-// freed.
+// Every hand-off is an mbarrier; every wait is bounded in time (kAttnWaitNs,
+// gtms_attn_bwd.cuh). If a wait runs out, the kernel ORs GTMS_ERR_TIMEOUT into
+// the caller's status word, every role leaves its loop, the copies and MMAs
+// already issued are waited for (bounded by kAttnDrainWaitNs) and the tensor
+// memory is freed.
 #pragma once
 
 #include <cstdint>
@@ -47,6 +48,14 @@ constexpr int kTmaThreads = 32 * (kWarpZero0 + kZeroWarps);
 // Tile iterations by which the L2 prefetch of P runs ahead of the TMA loads
 // (measured on GB300: 0-2 is best, 6 and more lose to L2 thrashing).
 constexpr uint32_t kPrefetchAhead = 1;
+
+// Test builds only: with GTMS_ATTN_TMA_NO_LOADS defined to 1 (a separate library
+// that the test suite compiles; never libgtms) the producer issues no copies, so
+// the consumers' waits run out and the kernel takes its give-up path.
+#ifndef GTMS_ATTN_TMA_NO_LOADS
+#define GTMS_ATTN_TMA_NO_LOADS 0
+#endif
+constexpr bool kAttnNoLoads = GTMS_ATTN_TMA_NO_LOADS != 0;
 
 template <int D>
 struct AttnTma {
@@ -83,14 +92,14 @@ __device__ __forceinline__ void attn_abort(AttnShared& sh, int32_t* status)
 {
     *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
     if (status)
-        atomicOr(status, 1);
+        atomicOr(status, GTMS_ERR_TIMEOUT);
 }
 
 // All 32 lanes wait; the verdict is the warp's (so that warp-collective
 // instructions that follow stay converged).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity)
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns)
 {
-    return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, kAttnWaitLimit)) != 0;
+    return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, limit_ns)) != 0;
 }
 
 struct AttnItem {
@@ -124,7 +133,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_ds,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                              T* dS, const int32_t* __restrict__ seq_lens, int32_t M, int32_t S, int32_t nrb,
-                             int64_t n_slices, int64_t group, float scale, int32_t* status)
+                             int64_t n_slices, int64_t group, float scale, int32_t* status, uint64_t wait_ns)
 {
     using IO = Pairs<T>;
     using TL = AttnTma<D>;
@@ -169,7 +178,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
 
     if (warp == kWarpProducer) {
         if (lane == 0) {
-            uint32_t g = 0, itm = 0, gv = 0, gp = 0;   // iterations; V and P loads issued
+            uint32_t g = 0, itm = 0, gv = 0, gp = 0, gd = 0;   // iterations, work items; V, P, dO loads issued
             bool ok = true;
             // A second cursor walks the same iterations kPrefetchAhead ahead of the
             // loads and prefetches the P tiles of pass 1 into L2, so that the TMA
@@ -194,12 +203,16 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                     continue;
                 const int32_t z = static_cast<int32_t>(it.slice);
                 const uint32_t p = itm & 1u;
-                ok = tc::mbar_wait(&sh.doempty[p], ((itm >> 1) & 1u) ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                ok = tc::mbar_wait(&sh.doempty[p], ((itm >> 1) & 1u) ^ 1u, wait_ns) && !attn_aborted(sh);
                 if (!ok)
                     break;
-                tc::mbar_arrive_expect_tx(&sh.dofull[p], TL::op);
-                for (int kc = 0; kc < D / 8; ++kc)
-                    tc::tma_load_3d(base + TL::off_do + p * TL::op + kc * TL::lbo, &tm_do, kc * 8, it.r0, z, &sh.dofull[p]);
+                if constexpr (!kAttnNoLoads) {
+                    tc::mbar_arrive_expect_tx(&sh.dofull[p], TL::op);
+                    for (int kc = 0; kc < D / 8; ++kc)
+                        tc::tma_load_3d(base + TL::off_do + p * TL::op + kc * TL::lbo, &tm_do, kc * 8, it.r0, z,
+                                        &sh.dofull[p]);
+                    gd = itm + 1;
+                }
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
                     const uint32_t sv = g % NV, phv = (g / NV) & 1u, sp = g % NP, php = (g / NP) & 1u;
                     const int32_t tc0 = (i < it.n_tiles ? i : i - it.n_tiles) * kAttnRows;
@@ -217,23 +230,28 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                             pf_live = pf_seek();
                         }
                     }
-                    ok = tc::mbar_wait(&sh.vempty[sv], phv ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                    ok = tc::mbar_wait(&sh.vempty[sv], phv ^ 1u, wait_ns) && !attn_aborted(sh);
                     if (!ok)
                         break;
-                    tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
-                    for (int kc = 0; kc < D / 8; ++kc)
-                        tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z, &sh.vfull[sv]);
-                    ++gv;
-                    ok = tc::mbar_wait(&sh.pempty[sp], php ^ 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                    if constexpr (!kAttnNoLoads) {
+                        tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
+                        for (int kc = 0; kc < D / 8; ++kc)
+                            tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z,
+                                            &sh.vfull[sv]);
+                        ++gv;
+                    }
+                    ok = tc::mbar_wait(&sh.pempty[sp], php ^ 1u, wait_ns) && !attn_aborted(sh);
                     if (!ok)
                         break;
-                    tc::mbar_arrive_expect_tx(&sh.pfull[sp], kAttnPTileBytes);
-                    ++gp;
-                    const uint32_t pt = base + TL::off_p + sp * kAttnPTileBytes;
-                    // Pass 1 keeps the P tile in L2 for pass 2, which is its last read.
-                    const uint64_t pol = i < it.n_tiles ? tc::policy_evict_last() : tc::policy_evict_first();
-                    tc::tma_load_3d(pt, &tm_p, tc0, it.r0, z, &sh.pfull[sp], pol);
-                    tc::tma_load_3d(pt + kAttnRows * 128, &tm_p, tc0 + 64, it.r0, z, &sh.pfull[sp], pol);
+                    if constexpr (!kAttnNoLoads) {
+                        tc::mbar_arrive_expect_tx(&sh.pfull[sp], kAttnPTileBytes);
+                        ++gp;
+                        const uint32_t pt = base + TL::off_p + sp * kAttnPTileBytes;
+                        // Pass 1 keeps the P tile in L2 for pass 2, which is its last read.
+                        const uint64_t pol = i < it.n_tiles ? tc::policy_evict_last() : tc::policy_evict_first();
+                        tc::tma_load_3d(pt, &tm_p, tc0, it.r0, z, &sh.pfull[sp], pol);
+                        tc::tma_load_3d(pt + kAttnRows * 128, &tm_p, tc0 + 64, it.r0, z, &sh.pfull[sp], pol);
+                    }
                 }
                 ++itm;
             }
@@ -242,14 +260,14 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 // Let the copies already issued land before the CTA can exit.
                 for (uint32_t k = 0; k < static_cast<uint32_t>(NV) && k < gv; ++k) {
                     const uint32_t gk = gv - 1 - k;
-                    tc::mbar_wait(&sh.vfull[gk % NV], (gk / NV) & 1u, kAttnWaitLimit);
+                    tc::mbar_wait(&sh.vfull[gk % NV], (gk / NV) & 1u, kAttnDrainWaitNs);
                 }
                 for (uint32_t k = 0; k < static_cast<uint32_t>(NP) && k < gp; ++k) {
                     const uint32_t gk = gp - 1 - k;
-                    tc::mbar_wait(&sh.pfull[gk % NP], (gk / NP) & 1u, kAttnWaitLimit);
+                    tc::mbar_wait(&sh.pfull[gk % NP], (gk / NP) & 1u, kAttnDrainWaitNs);
                 }
-                if (itm > 0)
-                    tc::mbar_wait(&sh.dofull[(itm - 1) & 1u], ((itm - 1) >> 1) & 1u, kAttnWaitLimit);
+                if (gd > 0)
+                    tc::mbar_wait(&sh.dofull[(gd - 1) & 1u], ((gd - 1) >> 1) & 1u, kAttnDrainWaitNs);
             }
         }
     } else if (warp == kWarpMma) {
@@ -262,14 +280,14 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 if (it.n_tiles == 0)
                     continue;
                 const uint32_t p = itm & 1u;
-                ok = tc::mbar_wait(&sh.dofull[p], (itm >> 1) & 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                ok = tc::mbar_wait(&sh.dofull[p], (itm >> 1) & 1u, wait_ns) && !attn_aborted(sh);
                 if (!ok)
                     break;
                 const uint32_t a_base = base + TL::off_do + p * TL::op;
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
                     const uint32_t sv = g % NV, phv = (g / NV) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
-                    ok = tc::mbar_wait(&sh.tempty[acc], pha ^ 1u, kAttnWaitLimit) &&
-                         tc::mbar_wait(&sh.vfull[sv], phv, kAttnWaitLimit) && !attn_aborted(sh);
+                    ok = tc::mbar_wait(&sh.tempty[acc], pha ^ 1u, wait_ns) &&
+                         tc::mbar_wait(&sh.vfull[sv], phv, wait_ns) && !attn_aborted(sh);
                     if (!ok)
                         break;
                     tc::fence_after_sync();
@@ -291,7 +309,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 attn_abort(sh, status);
             if (issued) {   // the last MMAs must complete before the tensor memory is freed
                 const uint32_t gl = g - 1;
-                tc::mbar_wait(&sh.tfull[gl & 1u], (gl >> 1) & 1u, kAttnWaitLimit);
+                tc::mbar_wait(&sh.tfull[gl & 1u], (gl >> 1) & 1u, kAttnDrainWaitNs);
             }
         }
     } else if (warp == kWarpStore) {
@@ -305,7 +323,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                     if (i < it.n_tiles)
                         continue;
                     const uint32_t s = g % NP;
-                    ok = tc::mbar_wait(&sh.dsready[s], (ds_par >> s) & 1u, kAttnWaitLimit) && !attn_aborted(sh);
+                    ok = tc::mbar_wait(&sh.dsready[s], (ds_par >> s) & 1u, wait_ns) && !attn_aborted(sh);
                     if (!ok)
                         break;
                     ds_par ^= 1u << s;
@@ -358,7 +376,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 const int32_t lim = live ? r - (tc0 + colq * 32) + 1 : 0;
                 const int kept = lim < 0 ? 0 : (lim > 32 ? 32 : lim);
                 const uint32_t s = g % NP, ph = (g / NP) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
-                ok = warp_wait(&sh.tfull[acc], pha) && !attn_aborted(sh);
+                ok = warp_wait(&sh.tfull[acc], pha, wait_ns) && !attn_aborted(sh);
                 if (!ok)
                     break;
                 tc::fence_after_sync();
@@ -368,7 +386,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive(&sh.tempty[acc]);
-                ok = warp_wait(&sh.pfull[s], ph);   // the P tile
+                ok = warp_wait(&sh.pfull[s], ph, wait_ns);   // the P tile
                 if (!ok)
                     break;
                 uint8_t* p_row = smem + row_off + s * kAttnPTileBytes;
@@ -423,11 +441,11 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                             red[(colq - 1) * 2 * kAttnRows + row] = dot_hi;
                             red[(colq - 1) * 2 * kAttnRows + kAttnRows + row] = dot_lo;
                             tc::mbar_arrive(&sh.red_in);
-                            ok = warp_wait(&sh.red_out, rp);
+                            ok = warp_wait(&sh.red_out, rp, wait_ns);
                             dh = red[6 * kAttnRows + row];
                             dl = red[7 * kAttnRows + row];
                         } else {
-                            ok = warp_wait(&sh.red_in, rp);
+                            ok = warp_wait(&sh.red_in, rp, wait_ns);
                             float hi = dot_hi, lo = dot_lo;
 #pragma unroll
                             for (int k = 0; k < 3; ++k) {
@@ -512,7 +530,8 @@ inline int sm_count()
 // Persistent launch: one CTA per SM (at most one per work item).
 template <typename T, int D>
 cudaError_t launch_attn_dscores_tma(const void* P, const void* dO, const void* V, void* dS, const int32_t* seq_lens,
-                                    int64_t B, int64_t M, int64_t S, float scale, int32_t* status, cudaStream_t st)
+                                    int64_t B, int64_t M, int64_t S, float scale, int32_t* status, cudaStream_t st,
+                                    uint64_t wait_ns = kAttnWaitNs)
 {
     const uint64_t slices = static_cast<uint64_t>(B) * M;
     CUtensorMap tm_p, tm_ds, tm_v, tm_do;
@@ -533,11 +552,9 @@ cudaError_t launch_attn_dscores_tma(const void* P, const void* dO, const void* V
         return cudaErrorUnknown;
     const int64_t grid = n_items < nsm ? n_items : nsm;
     const int64_t group = (4 * grid + nrb - 1) / nrb;   // slices whose items make about 4 per CTA
-    kern<<<static_cast<unsigned>(grid), kTmaThreads, smem, st>>>(tm_p, tm_ds, tm_v, tm_do, static_cast<T*>(dS),
-                                                                 seq_lens, static_cast<int32_t>(M),
-                                                                 static_cast<int32_t>(S), nrb,
-                                                                 static_cast<int64_t>(slices), group, scale, status);
-    return cudaGetLastError();
+    return launch_kernel(kern, static_cast<unsigned>(grid), kTmaThreads, smem, st, tm_p, tm_ds, tm_v, tm_do,
+                         static_cast<T*>(dS), seq_lens, static_cast<int32_t>(M), static_cast<int32_t>(S), nrb,
+                         static_cast<int64_t>(slices), group, scale, status, wait_ns);
 }
 
 }  // namespace gtms

@@ -2,6 +2,6 @@
 #include "gtms_launch.cuh"
 
 namespace gtms {
-template void launch_backward<__nv_bfloat16, 2>(int, const void*, const void*, void*, const int32_t*, const Geom&, float,
+template cudaError_t launch_backward<__nv_bfloat16, 2>(int, const void*, const void*, void*, const int32_t*, const Geom&, float,
                                          cudaStream_t);
 }  // namespace gtms

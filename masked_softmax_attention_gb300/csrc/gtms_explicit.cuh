@@ -255,36 +255,44 @@ namespace gtms {
 // Explicit-mask launchers: the per-row vector variants of gtms_dispatch.h (the
 // forward with its own register caps, GTMS_EXF_VEC*).
 template <typename T>
-void launch_forward_explicit(int id, const void* x, void* y, const uint8_t* mask, int32_t mask_batches, const Geom& g,
-                             float scale, cudaStream_t st)
+cudaError_t launch_forward_explicit(int id, const void* x, void* y, const uint8_t* mask, int32_t mask_batches,
+                                    const Geom& g, float scale, cudaStream_t st)
 {
     const T* xp = static_cast<const T*>(x);
     T* yp = static_cast<T*>(y);
-#define GTMS_EX_FWD_CASE(vid, tw, nv, mb) \
-    case vid: gtms_fwd_explicit_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows / (g.rows_per_b / g.S)), block_for<tw>(), 0, st>>>(xp, yp, mask, mask_batches, g, scale); break;
+    const int64_t pairs = g.rows / (g.rows_per_b / g.S);   // (batch, row) pairs: one team each
+#define GTMS_EX_FWD_CASE(vid, tw, nv, mb)                                                                          \
+    case vid:                                                                                                      \
+        return launch_kernel(gtms_fwd_explicit_kernel<T, tw, nv, mb>, grid_for<tw>(pairs), block_for<tw>(), 0, st, \
+                             xp, yp, mask, mask_batches, g, scale);
     if constexpr (sizeof(T) == 4) {
         switch (id) { GTMS_EXF_VEC4(GTMS_EX_FWD_CASE) default: break; }
     } else {
         switch (id) { GTMS_EXF_VEC2(GTMS_EX_FWD_CASE) default: break; }
     }
 #undef GTMS_EX_FWD_CASE
+    return cudaErrorInvalidValue;   // no kernel for this variant id
 }
 
 template <typename T>
-void launch_backward_explicit(int id, const void* y, const void* dy, void* dx, const uint8_t* mask,
-                              int32_t mask_batches, const Geom& g, float scale, cudaStream_t st)
+cudaError_t launch_backward_explicit(int id, const void* y, const void* dy, void* dx, const uint8_t* mask,
+                                     int32_t mask_batches, const Geom& g, float scale, cudaStream_t st)
 {
     const T* yp = static_cast<const T*>(y);
     const T* gp = static_cast<const T*>(dy);
     T* dp = static_cast<T*>(dx);
-#define GTMS_EX_BWD_CASE(vid, tw, nv, mb) \
-    case vid: gtms_bwd_explicit_kernel<T, tw, nv, mb><<<grid_for<tw>(g.rows / (g.rows_per_b / g.S)), block_for<tw>(), 0, st>>>(yp, gp, dp, mask, mask_batches, g, scale); break;
+    const int64_t pairs = g.rows / (g.rows_per_b / g.S);
+#define GTMS_EX_BWD_CASE(vid, tw, nv, mb)                                                                          \
+    case vid:                                                                                                      \
+        return launch_kernel(gtms_bwd_explicit_kernel<T, tw, nv, mb>, grid_for<tw>(pairs), block_for<tw>(), 0, st, \
+                             yp, gp, dp, mask, mask_batches, g, scale);
     if constexpr (sizeof(T) == 4) {
         switch (id) { GTMS_BWD_VEC4(GTMS_EX_BWD_CASE) default: break; }
     } else {
         switch (id) { GTMS_BWD_VEC2(GTMS_EX_BWD_CASE) default: break; }
     }
 #undef GTMS_EX_BWD_CASE
+    return cudaErrorInvalidValue;   // no kernel for this variant id
 }
 
 }  // namespace gtms

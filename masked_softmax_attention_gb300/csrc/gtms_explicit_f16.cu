@@ -2,8 +2,8 @@
 #include "gtms_explicit.cuh"
 
 namespace gtms {
-template void launch_forward_explicit<__half>(int, const void*, void*, const uint8_t*, int32_t, const Geom&, float,
+template cudaError_t launch_forward_explicit<__half>(int, const void*, void*, const uint8_t*, int32_t, const Geom&, float,
                                           cudaStream_t);
-template void launch_backward_explicit<__half>(int, const void*, const void*, void*, const uint8_t*, int32_t,
+template cudaError_t launch_backward_explicit<__half>(int, const void*, const void*, void*, const uint8_t*, int32_t,
                                            const Geom&, float, cudaStream_t);
 }  // namespace gtms

@@ -2,5 +2,5 @@
 #include "gtms_launch.cuh"
 
 namespace gtms {
-template void launch_forward<__nv_bfloat16, 2>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+template cudaError_t launch_forward<__nv_bfloat16, 2>(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
 }  // namespace gtms

@@ -49,6 +49,31 @@
 
 namespace gtms {
 
+// Launch through cudaLaunchKernelEx and return that launch's own status. (A
+// triple-chevron launch reports only through cudaGetLastError, which would also
+// return, and clear, an error left behind by earlier unrelated work on the thread.)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                                 Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Time bounds of the waits on mbarriers, in nanoseconds of the GPU's global
+// timer. kAttnWaitNs bounds a wait in the main loop: one that runs out means
+// another role stopped making progress, and the kernel gives up (the host
+// entry point passes it; a test build passes a short one). kAttnDrainWaitNs
+// bounds, after giving up, each wait for a copy or an MMA already issued; those
+// complete unless the hardware itself failed, and a CTA whose drain wait runs
+// out exits with that operation still outstanding.
+constexpr uint64_t kAttnWaitNs = 1000000000ull;        // 1 s
+constexpr uint64_t kAttnDrainWaitNs = 2000000000ull;   // 2 s
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kWarpTeamBlock = 128;   // threads per CTA when a warp owns a row (4 rows per CTA)
 
@@ -227,10 +252,13 @@ __device__ __forceinline__ float max3(float a, float b, float c)
 // alternate two buffers per row). Lane l of every warp then takes pair l, and
 // two butterflies give the row's extreme E and sum S = sum_w s_w 2^((e_w - E) c)
 // (the same operations in every warp, so every thread gets the same E and S).
-// Returns this warp's output factor 2^((e_w - E) c) / S. A warp with no kept
-// element has s_w == 0 and takes no part (a NaN sum still propagates).
+// A warp with no kept element, or whose kept inputs are all infinite on the
+// far side of the extreme, has s_w == 0 and takes no part (a NaN sum still
+// propagates). Returns E in `ext` and 1 / S in `inv`: an output is then
+// 2^((x - E) c) / S, the formula of the per-row kernels.
 template <int TW>
-__device__ __forceinline__ float team_softmax_factor(float e_w, float s_w, float c, bool use_max, float* smem)
+__device__ __forceinline__ void team_softmax_stats(float e_w, float s_w, float c, bool use_max, float* smem,
+                                                   float& ext, float& inv)
 {
     constexpr int NW = TW / 32;
     const int l = threadIdx.x & 31;
@@ -251,7 +279,8 @@ __device__ __forceinline__ float team_softmax_factor(float e_w, float s_w, float
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
-    return s_w != 0.0f ? __fmul_rn(ex2(__fmul_rn(__fsub_rn(e_w, E), c)), __frcp_rn(S)) : 0.0f;
+    ext = E;
+    inv = __frcp_rn(S);
 }
 
 __device__ __forceinline__ float min3(float a, float b, float c)

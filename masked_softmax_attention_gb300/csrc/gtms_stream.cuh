@@ -16,7 +16,7 @@
 //          flash_decoding.py, the reduce kernel);
 //   pass 2 walks the batches in reverse order, so the units read last in
 //          pass 1 -- the ones most likely still in L2 -- are read first, and
-//          stores 2^((x - e_w) c) * f with f = 2^((e_w - E) c) / S.
+//          stores 2^((x - E) c) / S.
 // The backward is the same walk with the float-float dot of gtms_kernels.cuh
 // in pass 1 and dx = scale * y * (dy - d) in pass 2.
 //
@@ -75,7 +75,11 @@ __device__ __forceinline__ void stream_fold(const Unit16 (&raw)[U], const UnitRa
     if (mb == neutral)
         return;   // no kept element of this thread in the batch
     const float mn = use_max ? fmaxf(m, mb) : fminf(m, mb);
-    if (l != 0.0f)
+    // Rescale only a non-empty sum whose extreme moved: an empty sum has no
+    // extreme yet (m is still the neutral infinity), and an unmoved extreme
+    // would cost an exponential for a factor of 1 -- or give NaN from
+    // inf - inf when the extreme is an infinite input.
+    if (l != 0.0f && m != mn)
         l = __fmul_rn(l, ex2(__fmul_rn(__fsub_rn(m, mn), c)));
     m = mn;
     const float2 shift = splat2(-mn), c2 = splat2(c);
@@ -103,8 +107,8 @@ __device__ __forceinline__ void stream_fold(const Unit16 (&raw)[U], const UnitRa
     l = __fadd_rn(l, __fadd_rn(acc.x, acc.y));
 }
 
-// Pass 2 of one batch: store y = 2^((x - e) c) * f for the kept units (masked
-// elements of partial units as +0.0).
+// Pass 2 of one batch: store y = 2^((x - e) c) * f for the kept units (e the
+// row's extreme, f = 1 / sum; masked elements of partial units as +0.0).
 template <typename T, int U, typename At>
 __device__ __forceinline__ void stream_store(char* row, const Unit16 (&raw)[U], const UnitRange& ur, At at, float e,
                                              float c, float f)
@@ -174,12 +178,15 @@ gtms_fwd_stream_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, G
             stream_fold<T, U>(raw, ur, at, c, use_max, m, l);
         }
 
-        // Merge (m, l) over the warp, then over the CTA: the factor turns an
-        // exponential taken against the warp's extreme into the output.
+        // Merge (m, l) over the warp, then over the CTA, into the row's extreme
+        // E and 1 / sum. (Pass 2 exponentiates against E, not against a warp's
+        // own extreme: a warp whose kept inputs are all -inf has e_w = -inf, and
+        // x - e_w would be NaN there.)
         const float e_w = use_max ? team_max<32>(m, nullptr) : -team_max<32>(-m, nullptr);
         const float part = l != 0.0f ? __fmul_rn(l, ex2(__fmul_rn(__fsub_rn(m, e_w), c))) : 0.0f;
         const float s_w = team_sum<32>(part, nullptr);
-        const float f = team_softmax_factor<TW>(e_w, s_w, c, use_max, red[par]);
+        float E, inv;
+        team_softmax_stats<TW>(e_w, s_w, c, use_max, red[par], E, inv);
         par ^= 1;
 
         // Pass 2, batches in reverse order.
@@ -187,7 +194,7 @@ gtms_fwd_stream_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, G
             const StreamBatch<TW, U> at{ur.u0 + i * kBatch + tid};
             Unit16 raw[U];
             load_kept<U>(xr, ur, at, raw);
-            stream_store<T, U>(yr, raw, ur, at, e_w, c, f);
+            stream_store<T, U>(yr, raw, ur, at, E, c, inv);
         }
     }
 }

@@ -199,6 +199,18 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, int32_t x, int32_
                  :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(src), "l"(pol) : "memory");
 }
 
+// Untiled bulk copy (TMA) of `bytes` bytes from global memory into this CTA's
+// shared memory, under an L2 cache policy; completion is signalled on the
+// mbarrier as transaction bytes. Both addresses 16-byte aligned, `bytes` a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint64_t* mbar,
+                                             uint64_t pol)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(mbar)), "l"(pol) : "memory");
+}
+
 // TMA: prefetch the box of a 3-D tensor map at (x, y, z) into L2 (no shared
 // memory, no completion signal), under an L2 cache policy.
 __device__ __forceinline__ void tma_prefetch_3d(const void* tmap, int32_t x, int32_t y, int32_t z, uint64_t pol)
@@ -225,16 +237,36 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Wait until the mbarrier's phase `parity` has completed, giving up after
-// `limit` polls (each poll may itself suspend for a short, hardware-chosen
-// time). Returns false if the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, int limit)
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t globaltimer_ns()
 {
-    uint32_t done = 0;
-    for (int it = 0; it < limit && !done; ++it)
-        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-                     : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done) : "r"(smem_u32(mbar)), "r"(parity) : "memory");
     return done != 0;
+}
+
+// Wait until the mbarrier's phase `parity` has completed, giving up once
+// `limit_ns` nanoseconds of the global timer have passed since the first poll
+// failed (each poll may itself suspend the thread for a short, hardware-chosen
+// time). Returns false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(mbar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    do {
+        if (mbar_try_wait(mbar, parity))
+            return true;
+    } while (globaltimer_ns() - t0 < limit_ns);
+    return false;
 }
 
 }  // namespace tc

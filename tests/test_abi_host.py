@@ -72,6 +72,7 @@ def test_version_and_status_strings(lib):
     assert gtms.status_string(INVALID) == "GTMS_ERR_INVALID_ARG"
     assert gtms.status_string(UNSUPPORTED) == "GTMS_ERR_UNSUPPORTED"
     assert gtms.status_string(gtms.GTMS_ERR_CUDA) == "GTMS_ERR_CUDA"
+    assert gtms.status_string(gtms.GTMS_ERR_TIMEOUT) == "GTMS_ERR_TIMEOUT"
     assert gtms.status_string(99) == "GTMS_UNKNOWN_STATUS"
 
 

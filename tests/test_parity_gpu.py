@@ -397,6 +397,33 @@ def test_long_rows_sampled(dev, S, dtype, L):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("S,dtype,scale", [(16384, "bf16", 0.125), (16384, "f32", -0.5), (2048, "bf16", 0.125),
+                                           (65536, "bf16", 0.125)])
+def test_infinite_inputs_before_the_extreme(dev, S, dtype, scale):
+    """Kept inputs at columns 1 .. 4999 are -inf (+inf for a negative scale), so their exponentials are 0:
+    the stream kernels' threads see whole batches of them before the first finite value (column 0 and
+    columns >= 5000), and their running sums must start cleanly, as the row-in-registers kernels do."""
+    inf = float("-inf") if scale > 0 else float("inf")
+    if S <= 16384:
+        w = si.custom(f"inf{S}", 2, 1, S, dtype, scale, seq_lens=(S, S // 2 + 1), x_std=2.0, seed=S + 41)
+        x = si.make_x(w, "cpu")
+        x[:, :, :, 1:5000] = inf
+        run_and_check(w, dev, x_cpu=x)
+        return
+    L = 40000   # one row of 64K elements: sampled rows against the oracle
+    w = si.custom(f"inf{S}", 1, 1, S, dtype, scale, seq_lens=(L,), x_std=2.0, seed=S + 41)
+    lens = si.seq_lens(w)
+    x = si.make_x(w, dev)
+    x[:, :, :, 1:5000] = inf
+    y = gtms.forward(x, torch.from_numpy(lens).to(dev), w.scale)
+    torch.cuda.synchronize()
+    st = Stats()
+    for r in (0, 1, 4999, 5000, 5001, 20000, L - 1, S - 1):
+        check_forward(to_bits(x[0, 0, r:r + 1], w.dtype).reshape(-1), to_bits(y[0, 0, r:r + 1], w.dtype).reshape(-1),
+                      lens, w.B, 1, S, w.scale, w.dtype, r, r + 1, st)
+    assert st.ok, f"forward {w.describe()}: {st}"
+
+
 SCALE_CASES = [(1000, "f32", -0.7), (2048, "bf16", -0.125), (37, "f16", -2.0), (4096, "f16", -0.25),
                (8192, "f32", -1.0), (16384, "bf16", -0.125), (1000, "f32", 0.0), (16384, "bf16", 0.0)]
 
@@ -723,6 +750,66 @@ def test_attention_softmax_backward_full_size_sampled(dev):
                     ds[b, m].reshape(1, 1, S, S), f"full size slice ({b},{m})")
     del p, ds, dout, v
     torch.cuda.empty_cache()
+
+
+def _build_give_up_probe():
+    """Compile tests/attn_give_up_probe.cu (the TMA attention kernel with its copies left out) into a
+    library of its own under _build/; libgtms.so is not touched."""
+    import ctypes
+    import os
+    import subprocess
+
+    from masked_softmax_attention_gb300 import _build as b
+
+    src = os.path.join(b.ROOT, "tests", "attn_give_up_probe.cu")
+    out_dir = os.path.join(b.ROOT, "_build", "test_probe")
+    os.makedirs(out_dir, exist_ok=True)
+    lib_path = os.path.join(out_dir, "libgtms_attn_give_up_probe.so")
+    deps = [src] + [os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC)] + [os.path.join(b.INCLUDE, "gtms.h")]
+    if not os.path.exists(lib_path) or any(os.path.getmtime(d) > os.path.getmtime(lib_path) for d in deps):
+        tmp = lib_path + f".{os.getpid()}.tmp"
+        subprocess.run([b.nvcc_path(), *b.ARCH, *b.NVCC_FLAGS, "-shared", src, "-o", tmp], check=True,
+                       capture_output=True, text=True)
+        os.replace(tmp, lib_path)
+    lib = ctypes.CDLL(lib_path)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.gtms_test_attn_no_loads.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, vp, vp,
+                                            ctypes.c_uint64]
+    lib.gtms_test_attn_no_loads.restype = ctypes.c_int
+    return lib
+
+
+def test_attention_kernel_gives_up_when_its_waits_run_out(dev):
+    """Failure detection of the TMA attention kernel, without a GPU fault: in a test build whose producer
+    issues no copies, every consumer wait runs out (after 200 us here). The launch must succeed, the
+    kernel must end promptly with GTMS_ERR_TIMEOUT in the status word, and the context must stay usable:
+    a normal call right after it matches the oracle."""
+    import time
+
+    probe = _build_give_up_probe()
+    B, M, S, d, dtype = 2, 4, 1024, 64, "bf16"
+    w, p_bits, dout, v = _attn_case(dev, B, M, S, d, dtype, (1024, 700), seed=97)
+    lens_d = torch.from_numpy(si.seq_lens(w)).to(dev)
+    p_d = from_bits(p_bits, dtype, "cpu").view(B, M, S, S).to(dev)
+    dout_d, v_d = dout.to(dev), v.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ds = torch.zeros_like(p_d)
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    rc = probe.gtms_test_attn_no_loads(p_d.data_ptr(), dout_d.data_ptr(), v_d.data_ptr(), ds.data_ptr(),
+                                       lens_d.data_ptr(), B, M, S, w.scale, status.data_ptr(),
+                                       torch.cuda.current_stream().cuda_stream, 200_000)
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert rc == 0
+    assert int(status.item()) == gtms.GTMS_ERR_TIMEOUT
+    assert elapsed < 20.0
+    status.zero_()
+    out = torch.full_like(p_d, float("nan"))
+    gtms.attention_softmax_backward(p_d, dout_d, v_d, lens_d, w.scale, out=out, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _attn_check(w, d, p_bits, dout, v, out, "after a give-up")
 
 
 @pytest.mark.parametrize("lens", [(0, 0), (-5, 3000)])
