@@ -674,6 +674,11 @@ def time_config(args, name, dev, stream, peak):
         mp = mask.data_ptr() if mask is not None else None
         keep += [x, y, mask]
         calls.append(("forward", lambda: fwd_c(xp, yp, lp, mp, sp), fb, kernel_label(gtms, w, 0)))
+        staged = gtms.kernel_name(2, w.S, w.dtype_code)
+        if mask is None and not w.mask_kind and staged != "none":
+            # the same forward by the staged kernel (rows brought into shared memory by TMA bulk copies)
+            calls.append(("forward_staged", lambda: lib.gtms_forward_staged(xp, yp, lp, w.B, w.M, w.S, float(w.scale),
+                                                                            w.dtype_code, sp), fb, staged))
         if w.backward:
             dy = si.make_dy(w, dev)
             dx = torch.empty_like(x)

@@ -118,6 +118,23 @@ int gtms_backward(const void* y, const void* dy, void* dx, const int32_t* seq_le
                   int64_t B, int64_t M, int64_t S, float scale, int dtype, void* stream);
 
 /*
+ * gtms_forward computed by the staged kernel: the block-per-row design of
+ * "优化ScaledMaskSoftmax算子" (sections 2.2 and 4.2: a thread block per row,
+ * the row staged in shared memory), with each live row's kept units brought
+ * into shared memory by one TMA bulk copy, several rows ahead of the row being
+ * reduced. Same operation, arguments and errors as gtms_forward, and the same
+ * output values within the parity tolerances. On GB300 it measured slower than
+ * gtms_forward (S = 2048 bf16: 5.6 against 6.4 TB/s), which stays the fast
+ * path; this entry point is kept for comparison and for other parts.
+ * GTMS_ERR_UNSUPPORTED beyond gtms_forward's cases: rows whose byte length is
+ * not a multiple of 16 or is 32 KB or more, buffers not 16-byte aligned.
+ * A copy that does not arrive within 1 s of GPU time is given up on: the row is
+ * then read straight from x (same result), never waited on forever.
+ */
+int gtms_forward_staged(const void* x, void* y, const int32_t* seq_lens,
+                        int64_t B, int64_t M, int64_t S, float scale, int dtype, void* stream);
+
+/*
  * Device address of a page-locked host buffer (allocated with cudaHostAlloc
  * or registered with cudaHostRegister), for passing host-resident tensors
  * straight to gtms_forward / gtms_backward: the kernels then read the kept
@@ -210,10 +227,11 @@ const char* gtms_status_string(int status);
 int gtms_version(void);
 
 /*
- * Name of the kernel variant that gtms_forward (direction 0) or
- * gtms_backward (direction 1) launches for this row length, dtype and
- * alignment (aligned16 != 0: every pointer is 16-byte aligned). Static string;
- * "none" for unsupported arguments. Host-only, enqueues nothing.
+ * Name of the kernel variant that gtms_forward (direction 0), gtms_backward
+ * (direction 1) or gtms_forward_staged (direction 2) launches for this row
+ * length, dtype and alignment (aligned16 != 0: every pointer is 16-byte
+ * aligned). Static string; "none" for unsupported arguments. Host-only,
+ * enqueues nothing.
  */
 const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16);
 

@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = ("gtms_forward", "gtms_backward", "gtms_status_string", "gtms
                     "gtms_device_pointer_of_host",
                     "gtms_forward_masked",
                     "gtms_backward_masked", "gtms_forward_explicit", "gtms_backward_explicit",
-                    "gtms_attention_softmax_backward")
+                    "gtms_attention_softmax_backward", "gtms_forward_staged")
 
 _lib = None
 _lock = threading.Lock()
@@ -62,6 +62,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.gtms_forward.restype = ctypes.c_int
         lib.gtms_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
         lib.gtms_backward.restype = ctypes.c_int
+        lib.gtms_forward_staged.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp]
+        lib.gtms_forward_staged.restype = ctypes.c_int
         lib.gtms_forward_masked.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, i64,
                                             ctypes.c_int, vp]
         lib.gtms_forward_masked.restype = ctypes.c_int
@@ -102,6 +104,10 @@ def gtms_forward(x, y, seq_lens, B, M, S, scale, dtype, stream) -> int:
 
 def gtms_backward(y, dy, dx, seq_lens, B, M, S, scale, dtype, stream) -> int:
     return load_library().gtms_backward(y, dy, dx, seq_lens, B, M, S, scale, dtype, stream)
+
+
+def gtms_forward_staged(x, y, seq_lens, B, M, S, scale, dtype, stream) -> int:
+    return load_library().gtms_forward_staged(x, y, seq_lens, B, M, S, scale, dtype, stream)
 
 
 def gtms_forward_masked(x, y, seq_lens, B, M, S, scale, mask_kind, window, dtype, stream) -> int:
@@ -202,6 +208,25 @@ def forward(x, seq_lens, scale: float = 1.0, out=None, mask_kind: int = GTMS_MAS
                              int(mask_kind), int(window), _dtype_code(x), stream)
     if rc != GTMS_OK:
         raise GtmsError("gtms_forward_masked", rc)
+    return y
+
+
+def forward_staged(x, seq_lens, scale: float = 1.0, out=None):
+    """``forward`` computed by the staged kernel (gtms_forward_staged: rows brought into shared
+    memory by TMA bulk copies); the same values within the parity tolerances."""
+    import torch
+
+    _check_scores("x", x)
+    B, M, S, _ = x.shape
+    _check_lens(seq_lens, B, x.device)
+    y = torch.empty_like(x) if out is None else out
+    if y.shape != x.shape or y.dtype != x.dtype or y.device != x.device or not y.is_contiguous():
+        raise ValueError("out must match x in shape, dtype, device and be contiguous")
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    rc = gtms_forward_staged(x.data_ptr(), y.data_ptr(), seq_lens.data_ptr(), B, M, S, float(scale), _dtype_code(x),
+                             stream)
+    if rc != GTMS_OK:
+        raise GtmsError("gtms_forward_staged", rc)
     return y
 
 

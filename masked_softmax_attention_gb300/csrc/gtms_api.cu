@@ -77,6 +77,14 @@ GTMS_EXTERN_ATTN_TMA(__nv_bfloat16, 128)
 GTMS_EXTERN_ATTN_TMA(__half, 64)
 GTMS_EXTERN_ATTN_TMA(__half, 128)
 #undef GTMS_EXTERN_ATTN_TMA
+template <typename T>
+cudaError_t launch_forward_staged(int, const void*, void*, const int32_t*, const Geom&, float, cudaStream_t);
+extern template cudaError_t launch_forward_staged<float>(int, const void*, void*, const int32_t*, const Geom&, float,
+                                                         cudaStream_t);
+extern template cudaError_t launch_forward_staged<__nv_bfloat16>(int, const void*, void*, const int32_t*, const Geom&,
+                                                                 float, cudaStream_t);
+extern template cudaError_t launch_forward_staged<__half>(int, const void*, void*, const int32_t*, const Geom&, float,
+                                                          cudaStream_t);
 }  // namespace gtms
 
 namespace {
@@ -242,6 +250,38 @@ GTMS_EXPORT int gtms_forward(const void* x, void* y, const int32_t* seq_lens, in
                              float scale, int dtype, void* stream)
 {
     return gtms_forward_masked(x, y, seq_lens, B, M, S, scale, GTMS_MASK_GROUPED_TRIL, 0, dtype, stream);
+}
+
+GTMS_EXPORT int gtms_forward_staged(const void* x, void* y, const int32_t* seq_lens, int64_t B, int64_t M,
+                                    int64_t S, float scale, int dtype, void* stream)
+{
+    const Checked c = check_shape(B, M, S, scale, dtype);
+    if (c.status != GTMS_OK || c.rows == 0)
+        return c.status;
+    const int e = elem_bytes(dtype);
+    if (!x || !y || !seq_lens)
+        return GTMS_ERR_INVALID_ARG;
+    if (!aligned_to(x, e) || !aligned_to(y, e) || !aligned_to(seq_lens, 4))
+        return GTMS_ERR_INVALID_ARG;
+    if (bad_alias(y, x, c.bytes) || overlaps(y, c.bytes, seq_lens, static_cast<uint64_t>(B) * 4))
+        return GTMS_ERR_INVALID_ARG;
+    const int variant = gtms::pick_staged_variant(S, e, aligned_to(x, 16) && aligned_to(y, 16));
+    if (variant < 0)
+        return GTMS_ERR_UNSUPPORTED;
+    gtms::Geom g;
+    g.rows = c.rows;
+    g.rows_per_b = M * S;
+    g.S = static_cast<int32_t>(S);
+    g.units = static_cast<int32_t>(S * e / 16);
+    g.small = c.rows <= static_cast<int64_t>(UINT32_MAX) ? 1 : 0;
+    g.window = static_cast<int32_t>(S);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (dtype) {
+    case GTMS_F32: return launch_status(gtms::launch_forward_staged<float>(variant, x, y, seq_lens, g, scale, st));
+    case GTMS_BF16:
+        return launch_status(gtms::launch_forward_staged<__nv_bfloat16>(variant, x, y, seq_lens, g, scale, st));
+    default: return launch_status(gtms::launch_forward_staged<__half>(variant, x, y, seq_lens, g, scale, st));
+    }
 }
 
 GTMS_EXPORT int gtms_backward_masked(const void* y, const void* dy, void* dx, const int32_t* seq_lens, int64_t B,
@@ -510,6 +550,25 @@ const KernelNames& kernel_names()
 
 GTMS_EXPORT const char* gtms_kernel_name(int direction, int64_t S, int dtype, int aligned16)
 {
+    if (direction == 2) {   // gtms_forward_staged
+        static const char* const kDtype[3] = {"f32", "bf16", "f16"};
+        struct Names {
+            char text[3][8][80];
+            Names()
+            {
+                for (int t = 0; t < 3; ++t)
+                    for (int i = 0; i < 3; ++i) {
+                        const gtms::StagedVariant v = gtms::staged_at(t == 0 ? 4 : 2, i);
+                        std::snprintf(text[t][i], sizeof text[t][i], "gtms_fwd_staged_kernel<%s,team%d,x%d,slots%d,minb%d>",
+                                      kDtype[t], v.team, v.per_thread, v.slots, v.min_ctas);
+                    }
+            }
+        };
+        static const Names names;
+        const int e = elem_bytes(dtype);
+        const int v = e == 0 ? -1 : gtms::pick_staged_variant(S, e, aligned16 != 0);
+        return v < 0 ? "none" : names.text[dtype][v];
+    }
     return gtms_kernel_name_masked(direction, S, dtype, aligned16, GTMS_MASK_GROUPED_TRIL, 0);
 }
 

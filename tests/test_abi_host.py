@@ -138,7 +138,16 @@ def test_kernel_choice(lib):
     assert gtms.kernel_name(0, 8193, F32) == "none"
     assert gtms.kernel_name(0, 65537, BF16) == "none"
     assert gtms.kernel_name(0, 0, F32) == "none"
-    assert gtms.kernel_name(2, 100, F32) == "none"
+    assert gtms.kernel_name(3, 100, F32) == "none"
+    # the staged forward (direction 2): a CTA team per row, rows of 16-byte units below 32 KB
+    assert gtms.kernel_name(2, 1000, F32) == "gtms_fwd_staged_kernel<f32,team64,x4,slots6,minb12>"
+    assert gtms.kernel_name(2, 2048, BF16) == "gtms_fwd_staged_kernel<bf16,team64,x4,slots2,minb10>"
+    assert gtms.kernel_name(2, 4096, BF16) == "gtms_fwd_staged_kernel<bf16,team128,x4,slots2,minb5>"
+    assert gtms.kernel_name(2, 8192, F16) == "gtms_fwd_staged_kernel<f16,team256,x4,slots2,minb3>"
+    assert gtms.kernel_name(2, 4096, F32) == "gtms_fwd_staged_kernel<f32,team256,x4,slots2,minb3>"
+    assert gtms.kernel_name(2, 8192, F32) == "none"      # 32 KB rows: stream rows
+    assert gtms.kernel_name(2, 1001, F32) == "none"      # not a 16-byte multiple
+    assert gtms.kernel_name(2, 1000, F32, aligned16=False) == "none"
     assert gtms.kernel_name(0, 100, 7) == "none"
 
 
@@ -210,6 +219,23 @@ def test_explicit_mask_arguments(lib):
         assert fn(*ptrs, MASK, 1, 2, 3, 8200, 1.0, F32, None) == UNSUPPORTED    # longer than 8192
         assert fn(*ptrs, MASK, 1, 0, 3, 64, 1.0, F32, None) == OK               # empty work
         assert fn(*ptrs, MASK, 1, 2, 3, 64, 1.0, 5, None) == UNSUPPORTED        # unknown dtype
+
+
+def test_staged_forward_arguments(lib):
+    fn = gtms.gtms_forward_staged
+
+    def call(x=X, y=Y, lens=LENS, B=2, M=3, S=64, scale=1.0, dtype=F32):
+        return fn(x, y, lens, B, M, S, scale, dtype, None)
+
+    assert call(B=-1) == INVALID and call(scale=float("nan")) == INVALID
+    assert call(dtype=3) == UNSUPPORTED
+    assert call(x=None) == INVALID and call(lens=None) == INVALID
+    assert call(y=X + 16) == INVALID                   # partial overlap of y with x
+    assert call(S=63) == UNSUPPORTED                   # rows not 16-byte multiples
+    assert call(x=X + 4) == UNSUPPORTED                # buffers only element-aligned
+    assert call(S=8192) == UNSUPPORTED                 # 32 KB rows (stream rows)
+    assert call(S=16384, dtype=BF16) == UNSUPPORTED
+    assert call(B=0, x=None, y=None, lens=None) == OK  # empty work
 
 
 @pytest.mark.parametrize("call", [fwd, bwd])

@@ -346,6 +346,115 @@ def test_host_pipeline_matches_device_calls(dev, chunk):
 
 
 # ---------------------------------------------------------------------------
+# Staged forward (gtms_forward_staged): each row's kept units brought into shared
+# memory by one TMA bulk copy, several rows ahead
+# ---------------------------------------------------------------------------
+
+STAGED = [
+    si.custom("st1000_f32", 2, 3, 1000, "f32", 1.0, seq_lens=(1000, 637), seed=111),
+    si.custom("st2048_bf16", 2, 2, 2048, "bf16", 0.125, seq_lens=(2048, 1500), x_std=2.0, seed=112),
+    si.custom("st4096_bf16", 2, 1, 4096, "bf16", 0.125, seq_lens=(4096, 3001), x_std=2.0, seed=113),
+    si.custom("st8192_f16", 1, 2, 8192, "f16", 0.125, seq_lens=(8192,), spike_prob=0.01, seed=114),
+    si.custom("st4096_f32", 2, 1, 4096, "f32", 0.7, seq_lens=(4096, 2049), seed=115),
+] + [si.custom(f"stedge{S}_{dt}", 5, 2, S, dt, -0.5 if S == 64 else 0.125, seq_lens=(-1, 0, 1, S // 2 + 1, S + 3),
+               x_std=2.0, seed=S + 116) for S, dt in ((8, "f32"), (64, "bf16"), (1024, "f16"), (1032, "f32"),
+                                                       (2056, "bf16"))]
+
+
+def _staged_run_and_check(w, dev, call=None, x_cpu=None):
+    """Full element-wise parity of a staged forward against the oracle; the output buffer starts as NaN,
+    so every element must be written."""
+    S = w.S
+    lens = si.seq_lens(w)
+    x = si.make_x(w, "cpu") if x_cpu is None else x_cpu
+    x_bits = to_bits(x, w.dtype).reshape(-1)
+    x_d = x.to(dev)
+    y = torch.full_like(x_d, float("nan"))
+    lens_d = torch.from_numpy(lens).to(dev)
+    if call is None:
+        gtms.forward_staged(x_d, lens_d, w.scale, out=y)
+    else:
+        call(x_d, y, lens_d)
+    torch.cuda.synchronize()
+    y_bits = to_bits(y, w.dtype).reshape(-1)
+    st = Stats()
+    for a, b in row_chunks(0, w.rows, S):
+        check_forward(x_bits[a * S:b * S], y_bits[a * S:b * S], lens, w.B, w.M, S, w.scale, w.dtype, a, b, st)
+    assert st.ok, f"staged forward {w.describe()}: {st}"
+    return y
+
+
+@pytest.mark.parametrize("w", STAGED, ids=[w.name for w in STAGED])
+def test_staged_forward_matches_oracle(dev, w):
+    _staged_run_and_check(w, dev)
+
+
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048), ("f16", 8192)])
+def test_staged_forward_agrees_with_forward_and_does_not_read_masked_inputs(dev, dtype, S):
+    """Where the staged kernel's team shape is the forward's (a team of 64 with 4 units per thread),
+    the arithmetic is the same, so the bits are; NaN in every masked input changes nothing."""
+    w = si.custom("staged_eq", 3, 2, S, dtype, 0.125, seq_lens=(S, S // 2 + 1, 0), seed=117)
+    lens_d = torch.from_numpy(si.seq_lens(w)).to(dev)
+    x = si.make_x(w, dev)
+    y = gtms.forward_staged(x, lens_d, w.scale)
+    nan = torch.tensor(float("nan"), dtype=x.dtype, device=dev)
+    y_nan = gtms.forward_staged(torch.where(_kept_mask(si.seq_lens(w), w.M, S, dev), x, nan), lens_d, w.scale)
+    torch.cuda.synchronize()
+    bits = torch.int32 if dtype == "f32" else torch.int16
+    assert torch.equal(y_nan.view(bits), y.view(bits))
+    if gtms.kernel_name(2, S, w.dtype_code).split(",")[1:3] == gtms.kernel_name(0, S, w.dtype_code).split(",")[1:3]:
+        assert torch.equal(y.view(bits), gtms.forward(x, lens_d, w.scale).view(bits))
+
+
+def _build_staged_give_up_probe():
+    """Compile tests/staged_give_up_probe.cu (the staged forward with no copy ever issued) into a library
+    of its own under _build/; libgtms.so is not touched."""
+    import ctypes
+    import os
+    import subprocess
+
+    from masked_softmax_attention_gb300 import _build as b
+
+    src = os.path.join(b.ROOT, "tests", "staged_give_up_probe.cu")
+    out_dir = os.path.join(b.ROOT, "_build", "test_probe")
+    os.makedirs(out_dir, exist_ok=True)
+    lib_path = os.path.join(out_dir, "libgtms_staged_give_up_probe.so")
+    deps = [src] + [os.path.join(b.CSRC, f) for f in os.listdir(b.CSRC)] + [os.path.join(b.INCLUDE, "gtms.h")]
+    if not os.path.exists(lib_path) or any(os.path.getmtime(d) > os.path.getmtime(lib_path) for d in deps):
+        tmp = lib_path + f".{os.getpid()}.tmp"
+        subprocess.run([b.nvcc_path(), *b.ARCH, *b.NVCC_FLAGS, "-shared", src, "-o", tmp], check=True,
+                       capture_output=True, text=True)
+        os.replace(tmp, lib_path)
+    lib = ctypes.CDLL(lib_path)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.gtms_test_staged_no_copies.argtypes = [vp, vp, vp, i64, i64, i64, ctypes.c_float, ctypes.c_int, vp,
+                                               ctypes.c_uint64]
+    lib.gtms_test_staged_no_copies.restype = ctypes.c_int
+    return lib
+
+
+@pytest.mark.parametrize("dtype,S", [("f32", 1000), ("bf16", 2048)])
+def test_staged_forward_gives_up_on_copies_that_never_arrive(dev, dtype, S):
+    """Failure path without a GPU fault: in a test build that issues no copy, every team's first wait
+    runs out (after 100 us), the team stops staging and reads its rows from global memory. The kernel
+    must end promptly and its output must still match the oracle element by element."""
+    import time
+
+    probe = _build_staged_give_up_probe()
+    w = si.custom("staged_give_up", 2, 4, S, dtype, 0.125, seq_lens=(S, S // 3 + 1), x_std=2.0, seed=118)
+    t0 = time.monotonic()
+
+    def call(x_d, y, lens_d):
+        rc = probe.gtms_test_staged_no_copies(x_d.data_ptr(), y.data_ptr(), lens_d.data_ptr(), w.B, w.M, S,
+                                              w.scale, w.dtype_code, torch.cuda.current_stream().cuda_stream,
+                                              100_000)
+        assert rc == 0
+
+    _staged_run_and_check(w, dev, call=call)
+    assert time.monotonic() - t0 < 60.0
+
+
+# ---------------------------------------------------------------------------
 # Long rows (up to S = 65536): rows of 32 KB and more stream in two passes, one CTA per row
 # ---------------------------------------------------------------------------
 
