@@ -735,12 +735,22 @@ def _attn_case(dev, B, M, S, d, dtype, lens, seed, scale=0.125):
 
 def _attn_check(w, d, p_bits, dout, v, ds_dev, tag):
     """Element-wise: masked entries +0.0 bits; kept entries within
-    ulp(ref) + scale * P * 2^-23 * (d * A_rc + (d + 3) * max_c' A_rc'), A = |dO| |V|^T.
-    d * 2^-23 * A bounds the fp32 accumulation of the d exact products of one dP
-    entry; through the row sum (P sums to 1 within bf16 / fp16 rounding, at most
-    1.004) that is d * 1.004 * 2^-23 * max A; the row sum's own fp32 unit sums
-    (a 4-long FMA chain per lane, then one add) add at most 5 * 2^-24 * max A.
-    The fp32 steps after the row sum are far inside the second half-ulp."""
+        ulp(ref) + scale * P_rc * 2^-23 * (d * A_rc + (d + 3) * max_c' A_rc' + (N_r - 1 + d / 8) * F_r),
+    with A = |dO| |V|^T, N_r = 128 * (r // 128) the columns left of the diagonal tile of row r's
+    128-row block, and F_r = sum over those columns of P_rc' A_rc'. Every addition inside the tensor
+    cores is taken to round with a relative error of at most 2^-23 (one ulp: round to nearest and
+    truncation both qualify), whatever the order:
+    * dP_rc sums d exact products: off by at most d * 2^-23 * A_rc, and that reaches dS_rc directly;
+    * the row sum over the diagonal tile (float-float over unit sums of 8 products, an FMA chain):
+      the same dP error weighted by P (which sums to at most 1.004 after 16-bit rounding) plus
+      5 * 2^-24 per unit sum, at most (d + 3) * 2^-23 * max A -- the whole row sum of the per-tile
+      form is bounded by this term too;
+    * the kernel that takes the columns left of the diagonal tile as dO_r . (P V)_r: (P V)_rk sums
+      N_r exact products, off by at most (N_r - 1) * 2^-23 * sum_c' P_rc' |V_c'k|, which the dot
+      with dO_r weights into (N_r - 1) * 2^-23 * F_r; the fp32 dot itself (d / 4 terms per thread,
+      FMA chain, merged as float-float) adds at most (d / 8) * 2^-23 * F_r.
+    The fp32 steps after the row sum are far inside the second half-ulp. The bound covers both kernels
+    (the per-tile row sum of the cp.async kernel is the case F_r weighted by zero)."""
     B, M, S, dt = w.B, w.M, w.S, w.dtype
     lens = si.seq_lens(w)
     code = w.dtype_code
@@ -755,12 +765,14 @@ def _attn_check(w, d, p_bits, dout, v, ds_dev, tag):
     kept = np.broadcast_to(kept, ref.shape)
     assert np.count_nonzero(got[~kept]) == 0, f"{tag}: masked output not +0.0"
     Amax = np.where(kept, A, 0.0).max(axis=-1, keepdims=True)
+    n_left = (128 * (np.arange(S) // 128))[None, None, :, None]          # N_r, per row
+    F = np.where(kept & (col < n_left), pv * A, 0.0).sum(axis=-1, keepdims=True)
     # one ulp of the IO dtype at |ref|: the gap to the next representable magnitude
     rb = oracle.round_to(np.abs(ref), code).astype(np.int64)
     top = 0x7BFF if dt == "f16" else 0x7F7F
     nb = np.where(rb < top, rb + 1, rb - 1)
     ulp = np.abs(oracle.decode(nb.astype(np.uint16), code) - oracle.decode(rb.astype(np.uint16), code))
-    tol = ulp + abs(w.scale) * pv * 2.0 ** -23 * (d * A + (d + 3) * Amax)
+    tol = ulp + abs(w.scale) * pv * 2.0 ** -23 * (d * A + (d + 3) * Amax + (np.maximum(n_left - 1, 0) + d / 8) * F)
     err = np.abs(oracle.decode(got, code) - ref)
     bad = kept & (err > tol)
     assert not bad.any(), f"{tag}: {int(bad.sum())} of {int(kept.sum())} kept entries out of tolerance, " \
