@@ -5,29 +5,44 @@
 // "ops(8): self-attention 的 CUDA 实现及优化 (下)", section 2.1:
 //   dP = dO V^T,  dS = scale * P * (dP - rowsum(dP * P))  over the kept set c <= r < L.
 //
+// Pass 1 forms the row sum. For the tiles left of the diagonal tile every entry
+// is kept, and sum_c dP_rc P_rc = dO_r . sum_c P_rc V_c, so those tiles go to the
+// tensor cores alone: O = P V accumulates in tensor memory (P the A operand
+// straight from its TMA stage, V the B operand read MN-major), with no epilogue
+// work per tile. Only the diagonal tile, whose masked entries must not be used
+// (they may hold anything), goes through the per-element row sum of dP * P.
+// The row sum is then D_r = (diagonal tile's sum) + dO_r . O_r. Pass 2
+// recomputes dP tile by tile and writes dS.
+//
 // One CTA per SM walks the (slice, 128-row block) work items (see attn_item
 // for their order). Its warps:
-//   producer (1 lane)  TMA loads, per tile iteration, the V tile into a ring of
-//                      NV stages (8-column boxes, no swizzle: K-adjacent core
-//                      matrices 2 KB apart) and the P tile into a ring of NP
-//                      stages (two 64-column boxes, 128-byte swizzle); once per
-//                      work item the dO rows (two buffers, so the next item's
-//                      can land early); and an L2 prefetch of the next P tile
-//                      before it waits for a free stage;
-//   MMA (1 lane)       tcgen05.mma dP tile = dO . V^T into one of two
-//                      tensor-memory accumulators, as soon as the V tile has
-//                      landed, committed to mbarriers that hand the accumulator
-//                      to the epilogue and the V stage back to the producer;
-//   epilogue (16 warps) warp w reads lanes 32 (w % 4) .. + 31 (its rows) and
-//                      columns 32 (w / 4) .. + 31 of the accumulator, and forms
-//                      the row sums (pass 1) or writes dS over P in the stage
-//                      (pass 2);
+//   producer (1 lane)  TMA loads, per tile iteration, the P tile into a ring of
+//                      NP stages (two 64-column boxes, 128-byte swizzle) and
+//                      the V tile into a ring of NV stages (8-column boxes, no
+//                      swizzle); once per work item the dO rows (two buffers,
+//                      so the next item's can land early); and an L2 prefetch
+//                      of the next P tile. A tile left of the diagonal whose
+//                      P stage last held a dP tile gets its V only once that
+//                      stage is free, so that the MMA, which waits on the
+//                      stage's P barrier for such tiles, never polls it a
+//                      phase behind;
+//   MMA (1 lane)       pass-1 tiles left of the diagonal: O += P . V into the
+//                      O columns of tensor memory, committed to the barriers
+//                      that free the P and V stages; the diagonal tile and the
+//                      pass-2 tiles: dP = dO . V^T into one of two accumulators,
+//                      committed to the barriers that hand it to the epilogue;
+//   epilogue (16 warps) first zero each block's columns right of its diagonal
+//                      tile (while the tensor cores run the tiles left of it);
+//                      then warp w reads lanes 32 (w % 4) .. + 31 (its rows)
+//                      and columns 32 (w / 4) .. + 31 of an accumulator: the
+//                      diagonal tile's row sums and, after it, its quarter of
+//                      O dotted with dO (pass 1), or dS written over P in the
+//                      stage (pass 2);
 //   store (1 lane)     TMA-stores each finished dS tile (rows past the tensor
 //                      are dropped by the TMA unit) and returns the stage;
-//   zero (2 warps)     zero-fill each block's columns right of the diagonal
-//                      tile, and whole padded row blocks.
+//   zero (2 warps)     zero-fill whole padded row blocks.
 // Every hand-off is an mbarrier; every wait is bounded in time (kAttnWaitNs,
-// gtms_attn_bwd.cuh). If a wait runs out, the kernel ORs GTMS_ERR_TIMEOUT into
+// gtms_kernels.cuh). If a wait runs out, the kernel ORs GTMS_ERR_TIMEOUT into
 // the caller's status word, every role leaves its loop, the copies and MMAs
 // already issued are waited for (bounded by kAttnDrainWaitNs) and the tensor
 // memory is freed.
@@ -73,12 +88,18 @@ struct AttnTma {
     static constexpr uint32_t sbo = 128;                            // row-adjacent core matrices
 };
 
+constexpr int kAttnTmemCols = 512;          // two 128-column dP accumulators, then O (64 or 128 columns)
+constexpr uint32_t kAttnOCol = 2 * kAttnRows;
+
 struct AttnShared {
-    uint64_t pfull[4], pempty[4], dsready[4];   // per P stage
+    uint64_t pfull[4], dsready[4];              // per P stage: loaded; dS written into it
+    uint64_t pepi[4], pmma[4];                  // per P stage: freed by the epilogue / store lane, or by the MMA
     uint64_t vfull[3], vempty[3];               // per V stage
-    uint64_t tfull[2], tempty[2];               // per accumulator
+    uint64_t tfull[2], tempty[2];               // per dP accumulator
+    uint64_t ofull, oempty;                     // the O accumulator (once per work item)
     uint64_t dofull[2], doempty[2];             // per dO buffer
     uint64_t red_in, red_out;                   // row-sum exchange between the column quarters
+    uint64_t mma_done;                          // every MMA issued has completed (before TMEM is freed)
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -138,6 +159,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
     using IO = Pairs<T>;
     using TL = AttnTma<D>;
     constexpr int NP = TL::NP, NV = TL::NV;
+    constexpr int DQ = D / 4;   // O columns per epilogue column quarter
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ AttnShared sh;
 
@@ -150,8 +172,9 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
     if (tid == 0) {
         for (int s = 0; s < NP; ++s) {
             tc::mbar_init(&sh.pfull[s], 1);
-            tc::mbar_init(&sh.pempty[s], kTmaEpiWarps);   // 16 epilogue warps, or the store lane x 16
             tc::mbar_init(&sh.dsready[s], kTmaEpiWarps);
+            tc::mbar_init(&sh.pepi[s], kTmaEpiWarps);   // 16 epilogue warps, or the store lane x 16
+            tc::mbar_init(&sh.pmma[s], 1);              // the MMA's commit
         }
         for (int s = 0; s < NV; ++s) {
             tc::mbar_init(&sh.vfull[s], 1);
@@ -163,13 +186,16 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
             tc::mbar_init(&sh.dofull[a], 1);
             tc::mbar_init(&sh.doempty[a], 1);
         }
+        tc::mbar_init(&sh.ofull, 1);
+        tc::mbar_init(&sh.oempty, kTmaEpiWarps);
         tc::mbar_init(&sh.red_in, 3 * kAttnRows);   // the threads of column quarters 1..3
         tc::mbar_init(&sh.red_out, kAttnRows);      // the threads of column quarter 0
+        tc::mbar_init(&sh.mma_done, 1);
         sh.abort_flag = 0;
     }
     if (warp == kWarpMma) {
         __syncwarp();
-        tc::tmem_alloc<2 * kAttnRows>(&sh.tmem_slot);
+        tc::tmem_alloc<kAttnTmemCols>(&sh.tmem_slot);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -179,6 +205,9 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
     if (warp == kWarpProducer) {
         if (lane == 0) {
             uint32_t g = 0, itm = 0, gv = 0, gp = 0, gd = 0;   // iterations, work items; V, P, dO loads issued
+            // Which barrier frees each P stage's latest tile (bit s set: the MMA's pmma[s], else pepi[s]),
+            // and the parity of the next phase to wait for on each.
+            uint32_t by_mma = 0, par_epi = 0, par_mma = 0;
             bool ok = true;
             // A second cursor walks the same iterations kPrefetchAhead ahead of the
             // loads and prefetches the P tiles of pass 1 into L2, so that the TMA
@@ -214,7 +243,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                     gd = itm + 1;
                 }
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
-                    const uint32_t sv = g % NV, phv = (g / NV) & 1u, sp = g % NP, php = (g / NP) & 1u;
+                    const uint32_t sv = g % NV, phv = (g / NV) & 1u, sp = g % NP, bit = 1u << sp;
                     const int32_t tc0 = (i < it.n_tiles ? i : i - it.n_tiles) * kAttnRows;
                     while (pf_live && pf_g <= g + kPrefetchAhead) {
                         if (pf_i < pf.n_tiles) {
@@ -230,19 +259,48 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                             pf_live = pf_seek();
                         }
                     }
-                    ok = tc::mbar_wait(&sh.vempty[sv], phv ^ 1u, wait_ns) && !attn_aborted(sh);
-                    if (!ok)
-                        break;
-                    if constexpr (!kAttnNoLoads) {
-                        tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
-                        for (int kc = 0; kc < D / 8; ++kc)
-                            tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z,
-                                            &sh.vfull[sv]);
-                        ++gv;
+                    // A tile left of the diagonal whose P stage last held a dP tile waits for
+                    // that stage before its V is issued: the MMA then waits on the stage's
+                    // P barrier, and must not find it a phase behind. Every other tile
+                    // issues its V first.
+                    const bool v_first = !(i < it.n_tiles - 1 && g >= static_cast<uint32_t>(NP) && !(by_mma & bit));
+                    if (v_first) {
+                        ok = tc::mbar_wait(&sh.vempty[sv], phv ^ 1u, wait_ns) && !attn_aborted(sh);
+                        if (!ok)
+                            break;
+                        if constexpr (!kAttnNoLoads) {
+                            tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
+                            for (int kc = 0; kc < D / 8; ++kc)
+                                tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z,
+                                                &sh.vfull[sv]);
+                            ++gv;
+                        }
                     }
-                    ok = tc::mbar_wait(&sh.pempty[sp], php ^ 1u, wait_ns) && !attn_aborted(sh);
-                    if (!ok)
-                        break;
+                    // The P stage: wait until its previous tile (g - NP) has been freed.
+                    if (g >= static_cast<uint32_t>(NP)) {
+                        if (by_mma & bit) {
+                            ok = tc::mbar_wait(&sh.pmma[sp], (par_mma >> sp) & 1u, wait_ns);
+                            par_mma ^= bit;
+                        } else {
+                            ok = tc::mbar_wait(&sh.pepi[sp], (par_epi >> sp) & 1u, wait_ns);
+                            par_epi ^= bit;
+                        }
+                        if (!(ok = ok && !attn_aborted(sh)))
+                            break;
+                    }
+                    by_mma = i < it.n_tiles - 1 ? by_mma | bit : by_mma & ~bit;   // tiles left of the diagonal
+                    if (!v_first) {
+                        ok = tc::mbar_wait(&sh.vempty[sv], phv ^ 1u, wait_ns) && !attn_aborted(sh);
+                        if (!ok)
+                            break;
+                        if constexpr (!kAttnNoLoads) {
+                            tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
+                            for (int kc = 0; kc < D / 8; ++kc)
+                                tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z,
+                                                &sh.vfull[sv]);
+                            ++gv;
+                        }
+                    }
                     if constexpr (!kAttnNoLoads) {
                         tc::mbar_arrive_expect_tx(&sh.pfull[sp], kAttnPTileBytes);
                         ++gp;
@@ -272,32 +330,59 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
         }
     } else if (warp == kWarpMma) {
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_f16<T>(kAttnRows, kAttnRows);
-            uint32_t g = 0, itm = 0;
+            constexpr uint32_t idesc_dp = tc::idesc_f16<T>(kAttnRows, kAttnRows);
+            constexpr uint32_t idesc_o = tc::idesc_f16<T>(kAttnRows, D) | tc::kIdescBMnMajor;
+            uint32_t g = 0, ga = 0, itm = 0;   // tile iterations, dP accumulations, work items
             bool ok = true, issued = false;
             for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
                 const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
                 if (it.n_tiles == 0)
                     continue;
                 const uint32_t p = itm & 1u;
-                ok = tc::mbar_wait(&sh.dofull[p], (itm >> 1) & 1u, wait_ns) && !attn_aborted(sh);
+                ok = tc::mbar_wait(&sh.dofull[p], (itm >> 1) & 1u, wait_ns) &&
+                     (itm == 0 || tc::mbar_wait(&sh.oempty, (itm - 1) & 1u, wait_ns)) && !attn_aborted(sh);
                 if (!ok)
                     break;
                 const uint32_t a_base = base + TL::off_do + p * TL::op;
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
-                    const uint32_t sv = g % NV, phv = (g / NV) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
-                    ok = tc::mbar_wait(&sh.tempty[acc], pha ^ 1u, wait_ns) &&
-                         tc::mbar_wait(&sh.vfull[sv], phv, wait_ns) && !attn_aborted(sh);
-                    if (!ok)
-                        break;
-                    tc::fence_after_sync();
-                    const uint32_t b_base = base + TL::off_v + sv * TL::op;
+                    const uint32_t sv = g % NV, phv = (g / NV) & 1u, sp = g % NP, php = (g / NP) & 1u;
+                    const uint32_t v_base = base + TL::off_v + sv * TL::op;
+                    if (i < it.n_tiles - 1) {
+                        // O += P . V: K = the tile's 128 columns, 8 steps of 16 (32 bytes of a
+                        // swizzled P row; 16 V rows, two core-matrix groups of 128 bytes).
+                        ok = tc::mbar_wait(&sh.vfull[sv], phv, wait_ns) && tc::mbar_wait(&sh.pfull[sp], php, wait_ns) &&
+                             !attn_aborted(sh);
+                        if (!ok)
+                            break;
+                        tc::fence_after_sync();
+                        const uint32_t p_base = base + TL::off_p + sp * kAttnPTileBytes;
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        tc::mma_f16(tmem + acc * kAttnRows, tc::smem_desc(a_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo),
-                                    tc::smem_desc(b_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo), idesc, ks > 0 ? 1u : 0u);
-                    tc::commit(&sh.tfull[acc]);
-                    tc::commit(&sh.vempty[sv]);
+                        for (int ks = 0; ks < kAttnRows / 16; ++ks)
+                            tc::mma_f16(tmem + kAttnOCol,
+                                        tc::smem_desc_sw128(p_base + (ks >> 2) * (kAttnRows * 128) + (ks & 3) * 32, 1024),
+                                        tc::smem_desc(v_base + ks * 256, 128, TL::lbo), idesc_o,
+                                        (i > 0 || ks > 0) ? 1u : 0u);
+                        tc::commit(&sh.pmma[sp]);
+                        tc::commit(&sh.vempty[sv]);
+                    } else {
+                        // dP = dO . V^T into accumulator ga % 2.
+                        const uint32_t acc = ga & 1u, pha = (ga >> 1) & 1u;
+                        ok = tc::mbar_wait(&sh.tempty[acc], pha ^ 1u, wait_ns) &&
+                             tc::mbar_wait(&sh.vfull[sv], phv, wait_ns) && !attn_aborted(sh);
+                        if (!ok)
+                            break;
+                        tc::fence_after_sync();
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks)
+                            tc::mma_f16(tmem + acc * kAttnRows, tc::smem_desc(a_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo),
+                                        tc::smem_desc(v_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo), idesc_dp,
+                                        ks > 0 ? 1u : 0u);
+                        tc::commit(&sh.tfull[acc]);
+                        tc::commit(&sh.vempty[sv]);
+                        if (i == it.n_tiles - 1)
+                            tc::commit(&sh.ofull);   // every O product of the item precedes this commit
+                        ++ga;
+                    }
                     issued = true;
                 }
                 if (!ok)
@@ -307,9 +392,9 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
             }
             if (!ok)
                 attn_abort(sh, status);
-            if (issued) {   // the last MMAs must complete before the tensor memory is freed
-                const uint32_t gl = g - 1;
-                tc::mbar_wait(&sh.tfull[gl & 1u], (gl >> 1) & 1u, kAttnDrainWaitNs);
+            if (issued) {   // every MMA must complete before the tensor memory is freed
+                tc::commit(&sh.mma_done);
+                tc::mbar_wait(&sh.mma_done, 0, kAttnDrainWaitNs);
             }
         }
     } else if (warp == kWarpStore) {
@@ -335,7 +420,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                         tc::tma_store_3d(&tm_ds, tc0 + 64, it.r0, z, pt + kAttnRows * 128, pol);
                     tc::bulk_commit();
                     tc::bulk_wait_read_all();
-                    tc::mbar_arrive(&sh.pempty[s], kTmaEpiWarps);
+                    tc::mbar_arrive(&sh.pepi[s], kTmaEpiWarps);
                 }
             }
             if (!ok)
@@ -343,49 +428,66 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
             tc::bulk_wait_all();
         }
     } else if (warp >= kWarpZero0) {
-        // Zero-fill warps: columns right of the diagonal tile, whole padded row blocks.
+        // Zero-fill warps: whole padded row blocks (the epilogue warps zero the
+        // columns right of the diagonal tile of the blocks that have tiles).
         const int zt = tid - kWarpZero0 * 32;
         for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
             if (attn_aborted(sh))
                 break;
             const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
+            if (it.n_tiles > 0)
+                continue;
             const int32_t r_end = it.r0 + kAttnRows < S ? it.r0 + kAttnRows : S;
-            const int32_t c_from = it.n_tiles * kAttnRows < S ? it.n_tiles * kAttnRows : S;
-            zero_region(dS + it.slice * static_cast<int64_t>(S) * S, S, it.r0, r_end, c_from, zt, kZeroWarps * 32);
+            zero_region(dS + it.slice * static_cast<int64_t>(S) * S, S, it.r0, r_end, 0, zt, kZeroWarps * 32);
         }
     } else {
-        // Epilogue warps 0..15: rows 32 (w % 4) + lane, columns 32 (w / 4) .. + 31 of each tile.
+        // Epilogue warps 0..15: rows 32 (w % 4) + lane, columns 32 (w / 4) .. + 31 of each dP tile
+        // (and O columns DQ (w / 4) .. + DQ - 1).
         const int quarter = warp & 3, colq = warp >> 2;
         const int row = quarter * 32 + lane;
         float* red = reinterpret_cast<float*>(smem + TL::off_red);
         const uint32_t row_off = TL::off_p + (colq >> 1) * (kAttnRows * 128) + row * 128;
         const int chunk0 = (colq & 1) * 4, rx = row & 7;
-        uint32_t g = 0, itm = 0;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t g = 0, ga = 0, itm = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
             if (it.n_tiles == 0)
                 continue;
+            // The block's columns right of its diagonal tile, zeroed by all 512 epilogue
+            // threads while the tensor cores run the tiles left of the diagonal.
+            {
+                const int32_t r_end = it.r0 + kAttnRows < S ? it.r0 + kAttnRows : S;
+                const int32_t c_from = it.n_tiles * kAttnRows < S ? it.n_tiles * kAttnRows : S;
+                zero_region(dS + it.slice * static_cast<int64_t>(S) * S, S, it.r0, r_end, c_from, tid,
+                            kTmaEpiWarps * 32);
+            }
             const int32_t r = it.r0 + row;
             const bool live = r < it.L;
             float dot_hi = 0.0f, dot_lo = 0.0f, dh = 0.0f, dl = 0.0f;
             for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
+                if (i < it.n_tiles - 1)
+                    continue;   // O tiles: tensor cores only
                 const bool pass2 = i >= it.n_tiles;
                 const int32_t tc0 = (pass2 ? i - it.n_tiles : i) * kAttnRows;
                 // Kept elements of this thread's 32 columns: the first `kept` of them.
                 const int32_t lim = live ? r - (tc0 + colq * 32) + 1 : 0;
                 const int kept = lim < 0 ? 0 : (lim > 32 ? 32 : lim);
-                const uint32_t s = g % NP, ph = (g / NP) & 1u, acc = g & 1u, pha = (g >> 1) & 1u;
+                const uint32_t s = g % NP, ph = (g / NP) & 1u, acc = ga & 1u, pha = (ga >> 1) & 1u;
+                ++ga;
                 ok = warp_wait(&sh.tfull[acc], pha, wait_ns) && !attn_aborted(sh);
                 if (!ok)
                     break;
                 tc::fence_after_sync();
                 float dp[32];
-                tc::tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kAttnRows + colq * 32, dp);
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0)
-                    tc::mbar_arrive(&sh.tempty[acc]);
+                tc::tmem_ld32(tmem + lane_base + acc * kAttnRows + colq * 32, dp);
+                if (pass2) {
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        tc::mbar_arrive(&sh.tempty[acc]);
+                }
                 ok = warp_wait(&sh.pfull[s], ph, wait_ns);   // the P tile
                 if (!ok)
                     break;
@@ -432,37 +534,77 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                     }
                 }
                 if (!pass2) {
+                    // The diagonal tile (the last of pass 1): its P stage is free again.
                     __syncwarp();
                     if (lane == 0)
-                        tc::mbar_arrive(&sh.pempty[s]);
-                    if (i == it.n_tiles - 1) {   // merge the four column quarters' row sums
-                        const uint32_t rp = itm & 1u;
-                        if (colq != 0) {
-                            red[(colq - 1) * 2 * kAttnRows + row] = dot_hi;
-                            red[(colq - 1) * 2 * kAttnRows + kAttnRows + row] = dot_lo;
-                            tc::mbar_arrive(&sh.red_in);
-                            ok = warp_wait(&sh.red_out, rp, wait_ns);
-                            dh = red[6 * kAttnRows + row];
-                            dl = red[7 * kAttnRows + row];
-                        } else {
-                            ok = warp_wait(&sh.red_in, rp, wait_ns);
-                            float hi = dot_hi, lo = dot_lo;
+                        tc::mbar_arrive(&sh.pepi[s]);
+                    // The tiles left of it: dO_r . O_r over this warp's DQ columns of O.
+                    ok = warp_wait(&sh.ofull, itm & 1u, wait_ns) && !attn_aborted(sh);
+                    if (!ok)
+                        break;
+                    tc::fence_after_sync();
+                    if (it.n_tiles > 1) {
+                        float o[DQ];
+                        if constexpr (DQ == 16)
+                            tc::tmem_ld16(tmem + lane_base + kAttnOCol + colq * DQ, o);
+                        else
+                            tc::tmem_ld32(tmem + lane_base + kAttnOCol + colq * DQ, o);
+                        if (live) {
+                            const uint8_t* do_row = smem + TL::off_do + (itm & 1u) * TL::op + row * 16;
+                            float acc_o = 0.0f;
 #pragma unroll
-                            for (int k = 0; k < 3; ++k) {
-                                float sum, err;
-                                two_sum(hi, red[k * 2 * kAttnRows + row], sum, err);
-                                hi = sum;
-                                lo = __fadd_rn(__fadd_rn(lo, red[k * 2 * kAttnRows + kAttnRows + row]), err);
+                            for (int j = 0; j < DQ / 8; ++j) {
+                                const uint4 raw = *reinterpret_cast<const uint4*>(
+                                    do_row + (colq * (DQ / 8) + j) * TL::lbo);
+                                const Unit16 du{{raw.x, raw.y, raw.z, raw.w}};
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const float2 d2 = IO::get(du, q);
+                                    acc_o = __fmaf_rn(d2.x, o[j * 8 + 2 * q], acc_o);
+                                    acc_o = __fmaf_rn(d2.y, o[j * 8 + 2 * q + 1], acc_o);
+                                }
                             }
-                            dh = __fadd_rn(hi, lo);
-                            dl = __fsub_rn(lo, __fsub_rn(dh, hi));
-                            red[6 * kAttnRows + row] = dh;
-                            red[7 * kAttnRows + row] = dl;
-                            tc::mbar_arrive(&sh.red_out);
+                            float sum, err;
+                            two_sum(dot_hi, acc_o, sum, err);
+                            dot_hi = sum;
+                            dot_lo = __fadd_rn(dot_lo, err);
                         }
-                        if (!ok)
-                            break;
                     }
+                    // O and dO read: the MMA may overwrite O, and reach the end of the item
+                    // (which frees the dO buffer) only after this accumulator is returned.
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::mbar_arrive(&sh.oempty);
+                        tc::mbar_arrive(&sh.tempty[acc]);
+                    }
+                    // Merge the four column quarters' row sums.
+                    const uint32_t rp = itm & 1u;
+                    if (colq != 0) {
+                        red[(colq - 1) * 2 * kAttnRows + row] = dot_hi;
+                        red[(colq - 1) * 2 * kAttnRows + kAttnRows + row] = dot_lo;
+                        tc::mbar_arrive(&sh.red_in);
+                        ok = warp_wait(&sh.red_out, rp, wait_ns);
+                        dh = red[6 * kAttnRows + row];
+                        dl = red[7 * kAttnRows + row];
+                    } else {
+                        ok = warp_wait(&sh.red_in, rp, wait_ns);
+                        float hi = dot_hi, lo = dot_lo;
+#pragma unroll
+                        for (int k = 0; k < 3; ++k) {
+                            float sum, err;
+                            two_sum(hi, red[k * 2 * kAttnRows + row], sum, err);
+                            hi = sum;
+                            lo = __fadd_rn(__fadd_rn(lo, red[k * 2 * kAttnRows + kAttnRows + row]), err);
+                        }
+                        dh = __fadd_rn(hi, lo);
+                        dl = __fsub_rn(lo, __fsub_rn(dh, hi));
+                        red[6 * kAttnRows + row] = dh;
+                        red[7 * kAttnRows + row] = dl;
+                        tc::mbar_arrive(&sh.red_out);
+                    }
+                    if (!ok)
+                        break;
                 } else {
                     tc::fence_smem_for_async();   // dS in the stage, visible to the TMA store
                     __syncwarp();
@@ -481,7 +623,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
     tc::fence_after_sync();
     if (warp == kWarpMma) {
         __syncwarp();
-        tc::tmem_free<2 * kAttnRows>(tmem);
+        tc::tmem_free<kAttnTmemCols>(tmem);
     }
 }
 

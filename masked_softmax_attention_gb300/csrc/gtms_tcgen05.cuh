@@ -34,9 +34,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            (static_cast<uint64_t>((sbo & 0x3FFFFu) >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 
+// Shared-memory matrix descriptor of a K-major operand stored with the 128-byte
+// swizzle (the layout a TMA load with SWIZZLE_128B writes): rows of 128 bytes,
+// 16-byte chunk j of row r at chunk j ^ (r % 8), 8-row groups `sbo` bytes apart;
+// layout type 2 (128-byte swizzle) in bits 61-63. The atom base must be
+// 1024-byte aligned; a K step inside the 128-byte row advances the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo)
+{
+    return smem_desc(addr, 16, sbo) | (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
 // of the same 16-bit type (bits 7-9 and 10-12: 0 = fp16, 1 = bf16), both
-// K-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// K-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28. (Bit 16 set makes B
+// MN-major: see kIdescBMnMajor.)
 template <typename T>
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
 {
@@ -44,6 +55,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
     return (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
+
+// Instruction-descriptor bit of a B operand stored MN-major (N contiguous in
+// each 16-byte row of a core matrix). In the no-swizzle MN-major layout the
+// descriptor's LBO is then the byte stride between core matrices adjacent
+// along K, and SBO between those adjacent along N (checked on GB300 with a
+// one-tile product against a CPU reference).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 
 // D (tensor memory) = A * B^T (+ D when accumulate != 0); issued by one thread.
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -80,6 +98,22 @@ template <int NCOLS>
 __device__ __forceinline__ void tmem_free(uint32_t taddr)
 {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "n"(NCOLS) : "memory");
+}
+
+// Warp-collective: 16 consecutive fp32 columns of this thread's lane, then wait
+// (load and wait in one statement, so no use of the values can move above the wait).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(taddr) : "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        v[j] = __uint_as_float(r[j]);
 }
 
 // Warp-collective: 32 consecutive fp32 columns of this thread's lane, then wait
