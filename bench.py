@@ -69,6 +69,20 @@ def required_bytes(w, lens, kept_total=None):
     return fwd, bwd
 
 
+def touched_bytes(w, mask):
+    """(forward, backward) bytes that the explicit-mask kernels move at 16-byte granularity: every
+    16-byte unit of x (of y and dy) that holds a kept element, the uint8 mask once, every output. With
+    scattered keep bits most units hold one, so this exceeds the kept-element count of required_bytes,
+    and it is the least any kernel that reads whole units can move."""
+    import torch
+
+    epu = 16 // w.elem_bytes
+    units = int(torch.count_nonzero(mask.view(w.B, w.S, w.S // epu, epu).amax(dim=-1)).item()) * w.M
+    dense = w.B * w.M * w.S * w.S * w.elem_bytes
+    mask_bytes = w.B * w.S * w.S
+    return 16 * units + mask_bytes + dense, 32 * units + mask_bytes + dense
+
+
 def entry_points(lib, w):
     """The C calls of one step of workload w: fwd(x, y, lens, mask, stream) and
     bwd(y, dy, dx, lens, mask, stream) (pointers as ints; mask used by explicit-mask
@@ -627,8 +641,8 @@ def run_e2e_attention_host_resident(args, w, lens, p, dout, v, stream, fn):
 # run): every listed configuration besides the headline one, the S = 4096 point,
 # the long rows, the other mask families, the explicit mask and the attention step.
 CONFIG_TABLE = ("worked_example", "s1000_b3", "s2048_bf16", "s8192_f16", "s4096_bf16", "s16384_bf16",
-                "s32768_bf16", "length_s2048_bf16", "window_s2048_bf16", "explicit_s2048_bf16",
-                "attn_s2048_bf16")
+                "s32768_bf16", "s65536_bf16", "s65536_f32", "length_s2048_bf16", "window_s2048_bf16",
+                "explicit_s2048_bf16", "attn_s2048_bf16")
 L2_BYTES = 129 * 1000 * 1000
 
 
@@ -690,6 +704,7 @@ def time_config(args, name, dev, stream, peak):
     if tensor_bytes <= L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
     entry = {"workload": w.name + ": " + w.describe()}
+    touched = touched_bytes(w, mask) if w.head_dim == 0 and w.keep_prob > 0 else None
     windows = []
     for label, call, nbytes, kname in calls:
         for _ in range(args.warmup):
@@ -720,6 +735,10 @@ def time_config(args, name, dev, stream, peak):
                         "frac_of_peak": round(gbs / peak, 4)}
         if flush is not None:
             entry[label]["l2"] = "flushed before every timed call (tensors smaller than L2); latency only"
+        if touched is not None:   # the same time on the bytes of whole 16-byte units touched
+            tb = touched[0 if label == "forward" else 1]
+            entry[label]["touched_bytes"] = tb
+            entry[label]["frac_of_peak_touched"] = round(tb / (statistics.fmean(ms) * 1e-3) / 1e9 / peak, 4)
     if status is not None and int(status.item()):
         raise RuntimeError(f"{name}: a bounded wait inside the attention kernel ran out")
     del keep, calls, flush

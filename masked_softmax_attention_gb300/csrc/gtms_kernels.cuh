@@ -309,6 +309,39 @@ __device__ __forceinline__ void store16(void* p, const Unit16& u)
     *reinterpret_cast<uint4*>(p) = make_uint4(u.w[0], u.w[1], u.w[2], u.w[3]);
 }
 
+// 16-byte load and store under an L2 cache policy (createpolicy): data read
+// again soon can be kept (evict_last), data not read again let go first.
+__device__ __forceinline__ Unit16 load16_hint(const void* p, uint64_t pol)
+{
+    Unit16 u;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(u.w[0]), "=r"(u.w[1]), "=r"(u.w[2]), "=r"(u.w[3])
+                 : "l"(p), "l"(pol)
+                 : "memory");
+    return u;
+}
+
+__device__ __forceinline__ void store16_hint(void* p, const Unit16& u, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+                 :: "l"(p), "r"(u.w[0]), "r"(u.w[1]), "r"(u.w[2]), "r"(u.w[3]), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 template <typename T> struct Pairs;
 
 template <> struct Pairs<float> {
@@ -589,7 +622,8 @@ __device__ __forceinline__ void bwd_dot(Unit16 (&ry)[NV], Unit16 (&rg)[NV], cons
 // bits at masked elements.
 template <typename T, int NV, typename UnitOf>
 __device__ __forceinline__ void bwd_store(char* row, const Unit16 (&ry)[NV], const Unit16 (&rg)[NV],
-                                          const UnitRange& ur, UnitOf unit_of, float dh, float dl, float scale)
+                                          const UnitRange& ur, UnitOf unit_of, float dh, float dl, float scale,
+                                          uint64_t pol = 0, bool hint = false)
 {
     using IO = Pairs<T>;
     constexpr int PPU = IO::kPairs, EPU = 2 * PPU;
@@ -608,7 +642,10 @@ __device__ __forceinline__ void bwd_store(char* row, const Unit16 (&ry)[NV], con
             const int lo_e = ur.c0 - j * EPU, hi_e = ur.c1 - j * EPU;
             if (lo_e > 0 || hi_e < EPU)
                 IO::clear_outside(o, lo_e, hi_e);
-            store16(row + 16 * j, o);
+            if (hint)
+                store16_hint(row + 16 * j, o, pol);
+            else
+                store16(row + 16 * j, o);
         }
     }
 }

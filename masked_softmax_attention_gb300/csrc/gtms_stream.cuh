@@ -22,7 +22,11 @@
 //
 // The kept units of a row are read twice; the second read is meant to hit L2
 // (the rows in flight hold far less than its 129 MB), so DRAM still sees each
-// kept byte about once. Zero stores of the masked units are issued first, as in the
+// kept byte about once. Cache policies make it so at the longest rows: pass 1
+// reads with evict_last, pass 2 reads and every store (zeros and outputs) with
+// evict_first, so the output stream does not push pass 1's lines out of L2
+// (measured on GB300 at S = 65536: forward 0.95 -> 0.99 and backward 0.91 ->
+// 0.96 of the copy rate in bf16, 1.00 -> 1.04 and 0.93 -> 0.98 in fp32). Zero stores of the masked units are issued first, as in the
 // other kernels. Every unit is loaded and stored by the same thread, so an
 // output may alias its input exactly.
 #pragma once
@@ -41,6 +45,19 @@ struct StreamBatch {
 // Element e of unit j lies in the kept range iff lo <= e < hi (lo = c0 - j*EPU,
 // hi = c1 - j*EPU); only the first and last kept units are partial.
 __device__ __forceinline__ bool in_range(int e, int lo, int hi) { return e >= lo && e < hi; }
+
+// Loads of the kept units of one batch under an L2 policy.
+template <int NV, typename UnitOf>
+__device__ __forceinline__ void load_kept_hint(const char* row, const UnitRange& ur, UnitOf unit_of, Unit16 (&raw)[NV],
+                                               uint64_t pol)
+{
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const int j = unit_of(k);
+        if (ur.kept(j))
+            raw[k] = load16_hint(row + 16 * j, pol);
+    }
+}
 
 // Pass 1 of one batch: fold the kept elements of the units at(k) into the
 // running extreme m and sum l. Values are decoded from the raw units twice (for
@@ -111,7 +128,7 @@ __device__ __forceinline__ void stream_fold(const Unit16 (&raw)[U], const UnitRa
 // row's extreme, f = 1 / sum; masked elements of partial units as +0.0).
 template <typename T, int U, typename At>
 __device__ __forceinline__ void stream_store(char* row, const Unit16 (&raw)[U], const UnitRange& ur, At at, float e,
-                                             float c, float f)
+                                             float c, float f, uint64_t pol)
 {
     using IO = Pairs<T>;
     constexpr int PPU = IO::kPairs, EPU = 2 * PPU;
@@ -135,7 +152,7 @@ __device__ __forceinline__ void stream_store(char* row, const Unit16 (&raw)[U], 
                 }
                 IO::put(o, p, __fmul2_rn(y, f2));
             }
-            store16(row + 16 * j, o);
+            store16_hint(row + 16 * j, o, pol);
         }
     }
 }
@@ -144,6 +161,8 @@ template <typename T, int MK, int TW, int U, int MINB>
 __global__ void __launch_bounds__(TW, MINB)
 gtms_fwd_stream_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
+    // L2 policies: pass 1's reads stay for pass 2; pass 2's reads and every store go first.
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     constexpr int EPU = 2 * Pairs<T>::kPairs;
     constexpr int kBatch = TW * U;
     __shared__ float red[2][2 * (TW / 32)];
@@ -162,9 +181,9 @@ gtms_fwd_stream_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, G
         char* yr = reinterpret_cast<char*>(y + q * g.S);
 
         for (int j = tid; j < ur.u0; j += TW)
-            store16(yr + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
+            store16_hint(yr + 16 * j, Unit16{{0u, 0u, 0u, 0u}}, drop);
         for (int j = ur.u1 + tid; j < g.units; j += TW)
-            store16(yr + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
+            store16_hint(yr + 16 * j, Unit16{{0u, 0u, 0u, 0u}}, drop);
         if (c1 <= c0)
             continue;   // uniform across the CTA
 
@@ -174,7 +193,7 @@ gtms_fwd_stream_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, G
         for (int i = 0; i < nb; ++i) {
             const StreamBatch<TW, U> at{ur.u0 + i * kBatch + tid};
             Unit16 raw[U];
-            load_kept<U>(xr, ur, at, raw);
+            load_kept_hint<U>(xr, ur, at, raw, keep);
             stream_fold<T, U>(raw, ur, at, c, use_max, m, l);
         }
 
@@ -193,8 +212,8 @@ gtms_fwd_stream_kernel(const T* x, T* y, const int32_t* __restrict__ seq_lens, G
         for (int i = nb - 1; i >= 0; --i) {
             const StreamBatch<TW, U> at{ur.u0 + i * kBatch + tid};
             Unit16 raw[U];
-            load_kept<U>(xr, ur, at, raw);
-            stream_store<T, U>(yr, raw, ur, at, E, c, inv);
+            load_kept_hint<U>(xr, ur, at, raw, drop);
+            stream_store<T, U>(yr, raw, ur, at, E, c, inv, drop);
         }
     }
 }
@@ -203,6 +222,7 @@ template <typename T, int MK, int TW, int U, int MINB>
 __global__ void __launch_bounds__(TW, MINB)
 gtms_bwd_stream_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict__ seq_lens, Geom g, float scale)
 {
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     constexpr int EPU = 2 * Pairs<T>::kPairs;
     constexpr int kBatch = TW * U;
     __shared__ float red[2][2 * (TW / 32)];
@@ -219,9 +239,9 @@ gtms_bwd_stream_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict
         char* dr = reinterpret_cast<char*>(dx + q * g.S);
 
         for (int j = tid; j < ur.u0; j += TW)
-            store16(dr + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
+            store16_hint(dr + 16 * j, Unit16{{0u, 0u, 0u, 0u}}, drop);
         for (int j = ur.u1 + tid; j < g.units; j += TW)
-            store16(dr + 16 * j, Unit16{{0u, 0u, 0u, 0u}});
+            store16_hint(dr + 16 * j, Unit16{{0u, 0u, 0u, 0u}}, drop);
         if (c1 <= c0)
             continue;
 
@@ -231,8 +251,8 @@ gtms_bwd_stream_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict
         for (int i = 0; i < nb; ++i) {
             const StreamBatch<TW, U> at{ur.u0 + i * kBatch + tid};
             Unit16 ry[U], rg[U];
-            load_kept<U>(yr, ur, at, ry);
-            load_kept<U>(gr, ur, at, rg);
+            load_kept_hint<U>(yr, ur, at, ry, keep);
+            load_kept_hint<U>(gr, ur, at, rg, keep);
             float bh, bl;
             bwd_dot<T, U>(ry, rg, ur, at, bh, bl);
             ff_merge(hi, lo, bh, bl);
@@ -246,9 +266,9 @@ gtms_bwd_stream_kernel(const T* y, const T* dy, T* dx, const int32_t* __restrict
         for (int i = nb - 1; i >= 0; --i) {
             const StreamBatch<TW, U> at{ur.u0 + i * kBatch + tid};
             Unit16 ry[U], rg[U];
-            load_kept<U>(yr, ur, at, ry);
-            load_kept<U>(gr, ur, at, rg);
-            bwd_store<T, U>(dr, ry, rg, ur, at, dh, dl, scale);
+            load_kept_hint<U>(yr, ur, at, ry, drop);
+            load_kept_hint<U>(gr, ur, at, rg, drop);
+            bwd_store<T, U>(dr, ry, rg, ur, at, dh, dl, scale, drop, true);
         }
     }
 }

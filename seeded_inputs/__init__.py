@@ -24,9 +24,11 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
   seq_len ~ U{2048..4096}, scale 0.125, forward + backward: an added S=4096
   measurement point mirroring the ScaledMaskSoftmax article's 4096 row.
 * ``s16384_bf16`` -- X[4,8,16384,16384] bf16 ~N(0, variance 4),
-  seq_len ~ U{8192..16384}, scale 0.125, and ``s32768_bf16`` --
-  X[1,4,32768,32768], seq_len ~ U{16384..32768}: added measurement points for
-  rows of 32 KB and more (the two-pass stream kernels).
+  seq_len ~ U{8192..16384}, scale 0.125, ``s32768_bf16`` --
+  X[1,4,32768,32768], seq_len ~ U{16384..32768}, and ``s65536_bf16`` /
+  ``s65536_f32`` -- X[1,2,65536,65536] bf16 / X[1,1,65536,65536] fp32,
+  seq_len ~ U{32768..65536}: added measurement points for rows of 32 KB and
+  more (the two-pass stream kernels), up to the longest rows served.
 * ``attn_s2048_bf16`` -- the attention-backward step at the ``s2048_bf16``
   shape: P the softmax of X[32,16,2048,2048] (bf16, variance 4,
   seq_len ~ U{1024..2048}, scale 0.125), dO and V [32,16,2048,64] ~ N(0,1).
@@ -136,6 +138,10 @@ WORKLOADS = {
                             seq_len_range=(8192, 16384), seed=20261210),
     "s32768_bf16": Workload("s32768_bf16", 1, 4, 32768, "bf16", 0.125, x_std=2.0,
                             seq_len_range=(16384, 32768), seed=20261211),
+    "s65536_bf16": Workload("s65536_bf16", 1, 2, 65536, "bf16", 0.125, x_std=2.0,
+                            seq_len_range=(32768, 65536), seed=20261217),
+    "s65536_f32": Workload("s65536_f32", 1, 1, 65536, "f32", 0.125, x_std=2.0,
+                           seq_len_range=(32768, 65536), seed=20261218),
     # attention-backward step (dS from P, dO, V) at the bf16 S = 2048 shape, head_dim 64
     "attn_s2048_bf16": Workload("attn_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
                                 seq_len_range=(1024, 2048), seed=20261212, head_dim=64),

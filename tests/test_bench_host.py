@@ -112,3 +112,19 @@ def test_fewer_than_three_warmup_steps_are_refused():
                           "worked_example", "--steps", "1", "--warmup", "2"],
                          capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0
+
+
+def test_touched_bytes_count_whole_units_with_a_kept_element():
+    """The explicit-mask byte model at 16-byte granularity, against a brute-force count of the units
+    that hold a kept element (bf16: 8 elements per unit), the mask and every output."""
+    w = dataclasses.replace(si.WORKLOADS["explicit_s2048_bf16"], B=2, M=3, S=64)
+    m = si.make_keep_mask(w, "cpu")
+    units = sum(int(m[b, r, 8 * j:8 * j + 8].any()) for b in range(w.B) for r in range(w.S) for j in range(w.S // 8))
+    dense = w.B * w.M * w.S * w.S * 2
+    fwd, bwd = bench.touched_bytes(w, m)
+    assert fwd == 16 * w.M * units + w.B * w.S * w.S + dense
+    assert bwd == 32 * w.M * units + w.B * w.S * w.S + dense
+    # never below the kept-element model: a unit read whole holds at least its kept elements
+    kept = int(m.count_nonzero()) * w.M
+    rf, rb = bench.required_bytes(w, si.seq_lens(w), kept)
+    assert fwd >= rf and bwd >= rb
