@@ -26,11 +26,11 @@
  * Ownership and threading. The caller owns every buffer. All tensor
  * pointers are addresses the current CUDA device can dereference: device
  * memory, or page-locked host memory mapped with gtms_device_pointer_of_host;
- * seq_lens is an int32[B] array in such memory. The library allocates nothing, keeps no per-call state, is
- * safe to call from several host threads, and never synchronises: work is
- * enqueued on `stream` (a cudaStream_t passed as void*; NULL is the legacy
- * default stream) and the call returns at once. The host never reads
- * seq_lens.
+ * seq_lens is an int32[B] array in such memory. The library allocates
+ * nothing, keeps no per-call state, is safe to call from several host
+ * threads, and never synchronises: work is enqueued on `stream` (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream) and the
+ * call returns at once. The host never reads seq_lens.
  *
  * Aliasing. Outputs may alias an input exactly (y == x; dx == dy or
  * dx == y): each row is read before that row is written. Partial overlap of
