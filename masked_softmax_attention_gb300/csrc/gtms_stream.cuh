@@ -26,9 +26,10 @@
 // reads with evict_last, pass 2 reads and every store (zeros and outputs) with
 // evict_first, so the output stream does not push pass 1's lines out of L2
 // (measured on GB300 at S = 65536: forward 0.95 -> 0.99 and backward 0.91 ->
-// 0.96 of the copy rate in bf16, 1.00 -> 1.04 and 0.93 -> 0.98 in fp32). Zero stores of the masked units are issued first, as in the
-// other kernels. Every unit is loaded and stored by the same thread, so an
-// output may alias its input exactly.
+// 0.96 of the copy rate in bf16, 1.00 -> 1.04 and 0.93 -> 0.98 in fp32).
+// Zero stores of the masked units are issued first, as in the other kernels.
+// Every unit is loaded and stored by the same thread, so an output may alias
+// its input exactly.
 #pragma once
 
 #include "gtms_kernels.cuh"
