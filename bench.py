@@ -642,7 +642,7 @@ def run_e2e_attention_host_resident(args, w, lens, p, dout, v, stream, fn):
 # the long rows, the other mask families, the explicit mask and the attention step.
 CONFIG_TABLE = ("worked_example", "s1000_b3", "s2048_bf16", "s8192_f16", "s4096_bf16", "s16384_bf16",
                 "s32768_bf16", "s65536_bf16", "s65536_f32", "length_s2048_bf16", "window_s2048_bf16",
-                "explicit_s2048_bf16", "attn_s2048_bf16")
+                "explicit_s2048_bf16", "attn_s2048_bf16", "attn_d128_s2048_f16")
 L2_BYTES = 129 * 1000 * 1000
 
 

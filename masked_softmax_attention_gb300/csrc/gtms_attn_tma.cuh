@@ -18,10 +18,13 @@
 // for their order). Its warps:
 //   producer (1 lane)  TMA loads, per tile iteration, the P tile into a ring of
 //                      NP stages (two 64-column boxes, 128-byte swizzle) and
-//                      the V tile into a ring of NV stages (8-column boxes, no
-//                      swizzle); once per work item the dO rows (two buffers,
-//                      so the next item's can land early); and an L2 prefetch
-//                      of the next P tile. A tile left of the diagonal whose
+//                      the V tile into a ring of NV stages; once per work item
+//                      the dO rows (at head dim 64 two buffers, so the next
+//                      item's can land early; one at 128); and an L2 prefetch
+//                      of the next P tile. V and dO travel as 8-column boxes
+//                      without swizzle at head dim 64, and as 64-column boxes
+//                      with the 128-byte swizzle at 128 (see AttnTma). A tile
+//                      left of the diagonal whose
 //                      P stage last held a dP tile gets its V only once that
 //                      stage is free, so that the MMA, which waits on the
 //                      stage's P barrier for such tiles, never polls it a
@@ -74,18 +77,41 @@ constexpr bool kAttnNoLoads = GTMS_ATTN_TMA_NO_LOADS != 0;
 
 template <int D>
 struct AttnTma {
-    // Stages of the P / dS ring and of the V ring: 213 KB of shared memory in
-    // all for head dim 64, 197 KB for 128.
-    static constexpr int NP = D == 64 ? 4 : 2;
+    // Stages of the P / dS ring, of the V ring and dO buffers: 213 KB of shared
+    // memory in all for head dim 64, 197 KB for 128. At 128 a V or dO tile is
+    // 32 KB, and one dO buffer buys a third P stage (measured on GB300 at
+    // [32,16,2048^2] fp16: 1.568 -> 1.539 ms).
+    static constexpr int NP = D == 64 ? 4 : 3;
     static constexpr int NV = D == 64 ? 3 : 2;
+    static constexpr int ND = D == 64 ? 2 : 1;
+    // V and dO as 64-column boxes with the 128-byte swizzle (one TMA row of 128
+    // bytes per tile row and box) instead of 8-column boxes of 16-byte rows.
+    // With 128 columns the 8-column boxes make 2048 TMA rows per V tile and
+    // limit the kernel: swizzled, 1.539 -> 1.333 ms. At 64 columns the
+    // swizzled form measured 3 % slower, so head dim 64 keeps the 8-column boxes.
+    static constexpr bool swizzled = D == 128;
     static constexpr uint32_t op = kAttnRows * D * 2;               // 128 rows of dO or V
     static constexpr uint32_t off_p = 0;                            // NP P / dS tiles (1024-aligned)
     static constexpr uint32_t off_v = NP * kAttnPTileBytes;         // NV V tiles
-    static constexpr uint32_t off_do = off_v + NV * op;             // 2 dO tiles
-    static constexpr uint32_t off_red = off_do + 2 * op;            // 8 x 128 floats: row-sum exchange
+    static constexpr uint32_t off_do = off_v + NV * op;             // ND dO tiles
+    static constexpr uint32_t off_red = off_do + ND * op;           // 8 x 128 floats: row-sum exchange
     static constexpr uint32_t bytes = off_red + 8 * kAttnRows * 4 + 1024;   // + slack to align the base
     static constexpr uint32_t lbo = kAttnRows * 16;                 // K-adjacent core matrices (one 8-column box)
     static constexpr uint32_t sbo = 128;                            // row-adjacent core matrices
+    static constexpr uint32_t box = kAttnRows * 128;                // one swizzled 64-column box (16 KB)
+
+    // TMA load of 128 rows of dO or V (row0 .. row0 + 127 of slice z) into dst.
+    __device__ static __forceinline__ void load_rows(uint32_t dst, const CUtensorMap* map, int32_t row0, int32_t z,
+                                                     uint64_t* bar)
+    {
+        if constexpr (swizzled) {
+            for (int kc = 0; kc < D / 64; ++kc)
+                tc::tma_load_3d(dst + kc * box, map, kc * 64, row0, z, bar);
+        } else {
+            for (int kc = 0; kc < D / 8; ++kc)
+                tc::tma_load_3d(dst + kc * lbo, map, kc * 8, row0, z, bar);
+        }
+    }
 };
 
 constexpr int kAttnTmemCols = 512;          // two 128-column dP accumulators, then O (64 or 128 columns)
@@ -231,15 +257,13 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 if (it.n_tiles == 0)
                     continue;
                 const int32_t z = static_cast<int32_t>(it.slice);
-                const uint32_t p = itm & 1u;
-                ok = tc::mbar_wait(&sh.doempty[p], ((itm >> 1) & 1u) ^ 1u, wait_ns) && !attn_aborted(sh);
+                const uint32_t p = itm % TL::ND;
+                ok = tc::mbar_wait(&sh.doempty[p], ((itm / TL::ND) & 1u) ^ 1u, wait_ns) && !attn_aborted(sh);
                 if (!ok)
                     break;
                 if constexpr (!kAttnNoLoads) {
                     tc::mbar_arrive_expect_tx(&sh.dofull[p], TL::op);
-                    for (int kc = 0; kc < D / 8; ++kc)
-                        tc::tma_load_3d(base + TL::off_do + p * TL::op + kc * TL::lbo, &tm_do, kc * 8, it.r0, z,
-                                        &sh.dofull[p]);
+                    TL::load_rows(base + TL::off_do + p * TL::op, &tm_do, it.r0, z, &sh.dofull[p]);
                     gd = itm + 1;
                 }
                 for (int32_t i = 0; i < 2 * it.n_tiles; ++i, ++g) {
@@ -270,9 +294,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                             break;
                         if constexpr (!kAttnNoLoads) {
                             tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
-                            for (int kc = 0; kc < D / 8; ++kc)
-                                tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z,
-                                                &sh.vfull[sv]);
+                            TL::load_rows(base + TL::off_v + sv * TL::op, &tm_v, tc0, z, &sh.vfull[sv]);
                             ++gv;
                         }
                     }
@@ -295,9 +317,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                             break;
                         if constexpr (!kAttnNoLoads) {
                             tc::mbar_arrive_expect_tx(&sh.vfull[sv], TL::op);
-                            for (int kc = 0; kc < D / 8; ++kc)
-                                tc::tma_load_3d(base + TL::off_v + sv * TL::op + kc * TL::lbo, &tm_v, kc * 8, tc0, z,
-                                                &sh.vfull[sv]);
+                            TL::load_rows(base + TL::off_v + sv * TL::op, &tm_v, tc0, z, &sh.vfull[sv]);
                             ++gv;
                         }
                     }
@@ -325,7 +345,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                     tc::mbar_wait(&sh.pfull[gk % NP], (gk / NP) & 1u, kAttnDrainWaitNs);
                 }
                 if (gd > 0)
-                    tc::mbar_wait(&sh.dofull[(gd - 1) & 1u], ((gd - 1) >> 1) & 1u, kAttnDrainWaitNs);
+                    tc::mbar_wait(&sh.dofull[(gd - 1) % TL::ND], ((gd - 1) / TL::ND) & 1u, kAttnDrainWaitNs);
             }
         }
     } else if (warp == kWarpMma) {
@@ -338,8 +358,8 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
                 if (it.n_tiles == 0)
                     continue;
-                const uint32_t p = itm & 1u;
-                ok = tc::mbar_wait(&sh.dofull[p], (itm >> 1) & 1u, wait_ns) &&
+                const uint32_t p = itm % TL::ND;
+                ok = tc::mbar_wait(&sh.dofull[p], (itm / TL::ND) & 1u, wait_ns) &&
                      (itm == 0 || tc::mbar_wait(&sh.oempty, (itm - 1) & 1u, wait_ns)) && !attn_aborted(sh);
                 if (!ok)
                     break;
@@ -357,11 +377,15 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                         tc::fence_after_sync();
                         const uint32_t p_base = base + TL::off_p + sp * kAttnPTileBytes;
 #pragma unroll
-                        for (int ks = 0; ks < kAttnRows / 16; ++ks)
+                        for (int ks = 0; ks < kAttnRows / 16; ++ks) {
+                            // V is the MN-major B operand: 16 V rows per K step, 256 bytes of 8-column boxes,
+                            // or 2048 bytes (two 8-row swizzle atoms) of the swizzled boxes.
+                            const uint64_t b_desc = TL::swizzled ? tc::smem_desc_sw128_mn(v_base + ks * 2048, TL::box)
+                                                                 : tc::smem_desc(v_base + ks * 256, 128, TL::lbo);
                             tc::mma_f16(tmem + kAttnOCol,
                                         tc::smem_desc_sw128(p_base + (ks >> 2) * (kAttnRows * 128) + (ks & 3) * 32, 1024),
-                                        tc::smem_desc(v_base + ks * 256, 128, TL::lbo), idesc_o,
-                                        (i > 0 || ks > 0) ? 1u : 0u);
+                                        b_desc, idesc_o, (i > 0 || ks > 0) ? 1u : 0u);
+                        }
                         tc::commit(&sh.pmma[sp]);
                         tc::commit(&sh.vempty[sv]);
                     } else {
@@ -373,10 +397,16 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                             break;
                         tc::fence_after_sync();
 #pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks)
-                            tc::mma_f16(tmem + acc * kAttnRows, tc::smem_desc(a_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo),
-                                        tc::smem_desc(v_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo), idesc_dp,
-                                        ks > 0 ? 1u : 0u);
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            // dO (A) and V (B) both K-major: a K step is 32 bytes of a swizzled 128-byte row
+                            // (the next box after four steps), or two 8-column boxes.
+                            const uint32_t koff = (ks >> 2) * TL::box + (ks & 3) * 32;
+                            const uint64_t a_desc = TL::swizzled ? tc::smem_desc_sw128(a_base + koff, 1024)
+                                                                 : tc::smem_desc(a_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo);
+                            const uint64_t b_desc = TL::swizzled ? tc::smem_desc_sw128(v_base + koff, 1024)
+                                                                 : tc::smem_desc(v_base + ks * 2 * TL::lbo, TL::lbo, TL::sbo);
+                            tc::mma_f16(tmem + acc * kAttnRows, a_desc, b_desc, idesc_dp, ks > 0 ? 1u : 0u);
+                        }
                         tc::commit(&sh.tfull[acc]);
                         tc::commit(&sh.vempty[sv]);
                         if (i == it.n_tiles - 1)
@@ -550,12 +580,14 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                         else
                             tc::tmem_ld32(tmem + lane_base + kAttnOCol + colq * DQ, o);
                         if (live) {
-                            const uint8_t* do_row = smem + TL::off_do + (itm & 1u) * TL::op + row * 16;
+                            const uint8_t* do_tile = smem + TL::off_do + (itm % TL::ND) * TL::op;
                             float acc_o = 0.0f;
 #pragma unroll
                             for (int j = 0; j < DQ / 8; ++j) {
-                                const uint4 raw = *reinterpret_cast<const uint4*>(
-                                    do_row + (colq * (DQ / 8) + j) * TL::lbo);
+                                const int k = colq * (DQ / 8) + j;   // 16-byte chunk of the dO row
+                                const uint32_t off = TL::swizzled ? (k >> 3) * TL::box + row * 128 + (((k & 7) ^ rx) << 4)
+                                                                  : k * TL::lbo + row * 16;
+                                const uint4 raw = *reinterpret_cast<const uint4*>(do_tile + off);
                                 const Unit16 du{{raw.x, raw.y, raw.z, raw.w}};
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {
@@ -679,8 +711,10 @@ cudaError_t launch_attn_dscores_tma(const void* P, const void* dO, const void* V
     CUtensorMap tm_p, tm_ds, tm_v, tm_do;
     if (!encode_map_3d(&tm_p, P, S, S, slices, 64, kAttnRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_map_3d(&tm_ds, dS, S, S, slices, 64, kAttnRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_map_3d(&tm_v, V, D, S, slices, 8, kAttnRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_map_3d(&tm_do, dO, D, S, slices, 8, kAttnRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !encode_map_3d(&tm_v, V, D, S, slices, AttnTma<D>::swizzled ? 64 : 8, kAttnRows,
+                       AttnTma<D>::swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_map_3d(&tm_do, dO, D, S, slices, AttnTma<D>::swizzled ? 64 : 8, kAttnRows,
+                       AttnTma<D>::swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     constexpr int smem = static_cast<int>(AttnTma<D>::bytes);
     auto* kern = gtms_attn_dscores_tma_kernel<T, D>;

@@ -44,6 +44,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t sbo)
     return smem_desc(addr, 16, sbo) | (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory matrix descriptor of an MN-major operand stored with the 128-byte
+// swizzle: each K row holds 64 16-bit MN elements in 128 bytes (chunks swizzled as
+// above), 8 K rows make a 1024-byte atom and the next 8 K rows follow it (SBO =
+// 1024); `lbo` is the byte stride between 64-element boxes along MN. A K step of
+// 16 advances the start address by 2048 bytes. (Checked on GB300 with a one-tile
+// product against a CPU reference, for N = 64 and 128.)
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t addr, uint32_t lbo)
+{
+    return smem_desc(addr, lbo, 1024) | (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and B
 // of the same 16-bit type (bits 7-9 and 10-12: 0 = fp16, 1 = bf16), both
 // K-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28. (Bit 16 set makes B

@@ -32,6 +32,9 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
 * ``attn_s2048_bf16`` -- the attention-backward step at the ``s2048_bf16``
   shape: P the softmax of X[32,16,2048,2048] (bf16, variance 4,
   seq_len ~ U{1024..2048}, scale 0.125), dO and V [32,16,2048,64] ~ N(0,1).
+* ``attn_d128_s2048_f16`` -- the same step in fp16 with head_dim 128: P the
+  softmax of X[32,16,2048,2048] (fp16, variance 4, seq_len ~ U{1024..2048},
+  scale 0.125), dO and V [32,16,2048,128] ~ N(0,1).
 * ``length_s2048_bf16``, ``window_s2048_bf16``, ``explicit_s2048_bf16`` -- the
   ``s2048_bf16`` shape and distribution under the length mask, a sliding causal
   window of width 256, and an explicit uint8 keep mask (``make_keep_mask``:
@@ -145,6 +148,9 @@ WORKLOADS = {
     # attention-backward step (dS from P, dO, V) at the bf16 S = 2048 shape, head_dim 64
     "attn_s2048_bf16": Workload("attn_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
                                 seq_len_range=(1024, 2048), seed=20261212, head_dim=64),
+    # the same step in fp16 with head_dim 128 (the kernel's other ring shape)
+    "attn_d128_s2048_f16": Workload("attn_d128_s2048_f16", 32, 16, 2048, "f16", 0.125, x_std=2.0,
+                                    seq_len_range=(1024, 2048), seed=20261219, head_dim=128),
     # the other mask families and an explicit keep mask, on the s2048_bf16 shape and distribution
     "length_s2048_bf16": Workload("length_s2048_bf16", 32, 16, 2048, "bf16", 0.125, x_std=2.0,
                                   seq_len_range=(1024, 2048), seed=20261214, mask_kind=1),

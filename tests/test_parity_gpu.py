@@ -842,10 +842,12 @@ def test_attention_softmax_backward_host_resident(dev, S, d, dtype, lens):
     _attn_check(w, d, p_bits, dout, v, ds_h, f"host S={S} d={d} {dtype}")
 
 
-def test_attention_softmax_backward_full_size_sampled(dev):
-    """The benchmark's workload (P[32,16,2048,2048] bf16, head dim 64) in the benchmark's launch: masked bits
-    zero everywhere; sampled slices, whose P is the oracle's own forward, element-wise against the oracle."""
-    w = si.WORKLOADS["attn_s2048_bf16"]
+@pytest.mark.parametrize("name", ["attn_s2048_bf16", "attn_d128_s2048_f16"])
+def test_attention_softmax_backward_full_size_sampled(dev, name):
+    """The benchmark's workloads (P[32,16,2048,2048] bf16 with head dim 64, fp16 with head dim 128) in the
+    benchmark's launch: masked bits zero everywhere; sampled slices, whose P is the oracle's own forward,
+    element-wise against the oracle."""
+    w = si.WORKLOADS[name]
     B, M, S, d = w.B, w.M, w.S, w.head_dim
     lens = si.seq_lens(w)
     lens_d = torch.from_numpy(lens).to(dev)
