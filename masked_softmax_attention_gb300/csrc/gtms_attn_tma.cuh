@@ -604,6 +604,10 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                     }
                     // O and dO read: the MMA may overwrite O, and reach the end of the item
                     // (which frees the dO buffer) only after this accumulator is returned.
+                    // That order rests on two accumulators: in an item of n >= 2 tiles the
+                    // second pass-2 dP product reuses this one, so the item's dO buffer is
+                    // committed free only after this read (n == 1 reads no dO). With a third
+                    // accumulator the next item's dO could land over this one first.
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
