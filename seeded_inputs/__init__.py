@@ -40,7 +40,8 @@ Workloads (shapes, dtypes and distributions of the pages' runs):
   window of width 256, and an explicit uint8 keep mask (``make_keep_mask``:
   each c <= r < seq_len entry kept with probability 1/2).
 * ``attn_s2048_b4`` -- ``attn_s2048_bf16`` with 4 batches: a profiler stand-in
-  (P and dS 537 MB each, still larger than L2).
+  (P and dS 537 MB each, still larger than L2); ``attn_d128_b4`` likewise for
+  ``attn_d128_s2048_f16``.
 * ``s1000_b2`` -- X[2,64,1000,1000], otherwise like ``s1000_b12``: a small
   stand-in for profiler captures.
 * ``s32768_m1`` -- X[1,1,32768,32768], otherwise like ``s32768_bf16`` (same
@@ -161,6 +162,8 @@ WORKLOADS = {
     # profiling stand-in for attn_s2048_bf16: same distribution, 4 of the 32 batches
     "attn_s2048_b4": Workload("attn_s2048_b4", 4, 16, 2048, "bf16", 0.125, x_std=2.0,
                               seq_len_range=(1024, 2048), seed=20261212, head_dim=64),
+    "attn_d128_b4": Workload("attn_d128_b4", 4, 16, 2048, "f16", 0.125, x_std=2.0,
+                             seq_len_range=(1024, 2048), seed=20261219, head_dim=128),
     # profiling stand-in for s1000_b12: same distribution, 2 of the 12 batches
     # (2 GB on the device), small enough for a multi-pass ncu capture
     "s1000_b2": Workload("s1000_b2", 2, 64, 1000, "f32", 1.0, seq_len_range=(500, 1000), seed=20261209),
