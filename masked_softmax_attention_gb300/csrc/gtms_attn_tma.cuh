@@ -185,6 +185,9 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
     using IO = Pairs<T>;
     using TL = AttnTma<D>;
     constexpr int NP = TL::NP, NV = TL::NV;
+    static_assert(NP <= 4 && NV <= 3 && TL::ND <= 2 && TL::ND >= 1,
+                  "AttnShared holds barriers for at most 4 P stages, 3 V stages and 2 dO buffers");
+    static_assert(TL::bytes <= 227 * 1024 - sizeof(AttnShared), "shared memory of one CTA");
     constexpr int DQ = D / 4;   // O columns per epilogue column quarter
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ AttnShared sh;
