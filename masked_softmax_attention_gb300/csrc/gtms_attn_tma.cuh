@@ -20,15 +20,14 @@
 //                      NP stages (two 64-column boxes, 128-byte swizzle) and
 //                      the V tile into a ring of NV stages; once per work item
 //                      the dO rows (at head dim 64 two buffers, so the next
-//                      item's can land early; one at 128); and an L2 prefetch
-//                      of the next P tile. V and dO travel as 8-column boxes
-//                      without swizzle at head dim 64, and as 64-column boxes
-//                      with the 128-byte swizzle at 128 (see AttnTma). A tile
-//                      left of the diagonal whose
-//                      P stage last held a dP tile gets its V only once that
-//                      stage is free, so that the MMA, which waits on the
-//                      stage's P barrier for such tiles, never polls it a
-//                      phase behind;
+//                      item's can land early; one at 128); and at head dim 64
+//                      an L2 prefetch of the next P tile. V and dO travel as
+//                      8-column boxes without swizzle at head dim 64, and as
+//                      64-column boxes with the 128-byte swizzle at 128 (see
+//                      AttnTma). A tile left of the diagonal whose P stage
+//                      last held a dP tile gets its V only once that stage is
+//                      free, so that the MMA, which waits on the stage's P
+//                      barrier for such tiles, never polls it a phase behind;
 //   MMA (1 lane)       pass-1 tiles left of the diagonal: O += P . V into the
 //                      O columns of tensor memory, committed to the barriers
 //                      that free the P and V stages; the diagonal tile and the
@@ -64,7 +63,9 @@ constexpr int kTmaEpiWarps = 16;                          // 4 lane quarters x 4
 constexpr int kWarpProducer = 16, kWarpMma = 17, kWarpStore = 18, kWarpZero0 = 19, kZeroWarps = 2;
 constexpr int kTmaThreads = 32 * (kWarpZero0 + kZeroWarps);
 // Tile iterations by which the L2 prefetch of P runs ahead of the TMA loads
-// (measured on GB300: 0-2 is best, 6 and more lose to L2 thrashing).
+// (measured on GB300 at head dim 64: 0-2 is best, 6 and more lose to L2
+// thrashing). At head dim 128 the prefetch costs time (1.308 ms without it,
+// 1.328 one tile ahead, 1.359 two ahead), so that kernel does not prefetch.
 constexpr uint32_t kPrefetchAhead = 1;
 
 // Test builds only: with GTMS_ATTN_TMA_NO_LOADS defined to 1 (a separate library
@@ -90,6 +91,7 @@ struct AttnTma {
     // limit the kernel: swizzled, 1.539 -> 1.333 ms. At 64 columns the
     // swizzled form measured 3 % slower, so head dim 64 keeps the 8-column boxes.
     static constexpr bool swizzled = D == 128;
+    static constexpr bool prefetch = D == 64;                       // L2 prefetch of P (kPrefetchAhead)
     static constexpr uint32_t op = kAttnRows * D * 2;               // 128 rows of dO or V
     static constexpr uint32_t off_p = 0;                            // NP P / dS tiles (1024-aligned)
     static constexpr uint32_t off_v = NP * kAttnPTileBytes;         // NV V tiles
@@ -240,7 +242,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
             bool ok = true;
             // A second cursor walks the same iterations kPrefetchAhead ahead of the
             // loads and prefetches the P tiles of pass 1 into L2, so that the TMA
-            // loads into the ring find them there.
+            // loads into the ring find them there (head dim 64 only: TL::prefetch).
             const uint64_t pol_keep = tc::policy_evict_last();
             int64_t pf_item = blockIdx.x;
             AttnItem pf{};
@@ -254,7 +256,7 @@ gtms_attn_dscores_tma_kernel(const __grid_constant__ CUtensorMap tm_p, const __g
                 }
                 return false;
             };
-            bool pf_live = pf_seek();
+            bool pf_live = TL::prefetch && pf_seek();
             for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
                 const AttnItem it = attn_item(item, n_slices, group, nrb, M, S, seq_lens);
                 if (it.n_tiles == 0)
